@@ -1,0 +1,135 @@
+"""Seeded synthetic inputs for multi-head scaled dot-product attention.
+
+This module is shared by the tests, the benchmark and the smoke check, and by
+both sides of every parity comparison (the CUDA path and the CPU oracle).  It
+holds no step of the attention arithmetic: it only draws numbers and rounds
+them to the storage type.
+
+Recipe (the pages' own data, WMT14 batches of about 25K source and 25K target
+tokens bucketed by length, section 5.1 of "Attention Is All You Need", are not
+available here; these tensors stand in for them):
+
+* Q, K, V entries are i.i.d. N(0, 1), drawn as float32 with NumPy's PCG64
+  generator seeded 0 (Q), 1 (K), 2 (V), then rounded to bfloat16 with
+  round-to-nearest-even (the float32 workload keeps the float32 draws).
+  Unit-variance q and k are the premise of the scaling argument in section
+  3.2.1 (footnote: q.k then has mean 0 and variance d_k).
+* Per-sequence key lengths for encoder-decoder attention are integers uniform
+  on [64, n_k] inclusive, PCG64 seeded 3.
+* Layout is [B, h, n, d] contiguous (heads split as (h, seq, d)).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+MASK_NONE = 0
+MASK_CAUSAL = 1
+MASK_KEY_PADDING = 2
+
+SEED_Q, SEED_K, SEED_V, SEED_LENS = 0, 1, 2, 3
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One attention problem: shapes, mask and storage type."""
+
+    name: str
+    B: int
+    h: int
+    n_q: int
+    n_k: int
+    d: int
+    mask: int
+    dtype: str  # "bf16" or "f32"
+    lens_lo: int = 64
+    note: str = field(default="", compare=False)
+
+    @property
+    def scale(self) -> float:
+        """1/sqrt(d_k), the scaling of eq. (1)."""
+        return 1.0 / math.sqrt(self.d)
+
+
+# The workloads: the base model (d_model=512, h=8, d_k=d_v=64) and the big
+# model (d_model=1024, h=16, d_k=d_v=64) of "Attention Is All You Need",
+# Table 3, used the three ways section 3.2.3 lists.
+WORKLOADS = {
+    "tiny": Workload("tiny", 1, 8, 64, 64, 64, MASK_NONE, "f32",
+                     note="tiny encoder self-attention, float32"),
+    "base_enc": Workload("base_enc", 64, 8, 512, 512, 64, MASK_NONE, "bf16",
+                         note="base encoder self-attention"),
+    "base_dec": Workload("base_dec", 64, 8, 512, 512, 64, MASK_CAUSAL, "bf16",
+                         note="base decoder masked self-attention"),
+    "encdec": Workload("encdec", 64, 8, 384, 512, 64, MASK_KEY_PADDING, "bf16",
+                       note="base encoder-decoder attention, key padding"),
+    "big": Workload("big", 8, 16, 4096, 4096, 64, MASK_NONE, "bf16",
+                    note="big model, long sequence, unmasked"),
+    "big_causal": Workload("big_causal", 8, 16, 4096, 4096, 64, MASK_CAUSAL,
+                           "bf16", note="big model, long sequence, causal"),
+}
+
+
+def gaussian(shape, seed: int) -> torch.Tensor:
+    """i.i.d. N(0,1) float32 on the CPU from PCG64(seed)."""
+    rng = np.random.default_rng(seed)
+    return torch.from_numpy(rng.standard_normal(size=tuple(shape), dtype=np.float32))
+
+
+def key_lengths(B: int, lo: int, hi: int, seed: int = SEED_LENS) -> torch.Tensor:
+    """B integers uniform on [lo, hi] inclusive, int32 on the CPU."""
+    rng = np.random.default_rng(seed)
+    return torch.from_numpy(rng.integers(lo, hi, size=B, endpoint=True).astype(np.int32))
+
+
+def make_inputs(w: Workload, device="cpu", seeds=(SEED_Q, SEED_K, SEED_V, SEED_LENS)):
+    """(q, k, v, key_lens) for a workload.
+
+    q, k, v are bfloat16 (or float32) tensors on ``device``; key_lens is an
+    int32 tensor on ``device`` for key padding, else None.
+    """
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    q = gaussian((w.B, w.h, w.n_q, w.d), seeds[0]).to(dt)
+    k = gaussian((w.B, w.h, w.n_k, w.d), seeds[1]).to(dt)
+    v = gaussian((w.B, w.h, w.n_k, w.d), seeds[2]).to(dt)
+    lens = None
+    if w.mask == MASK_KEY_PADDING:
+        lens = key_lengths(w.B, min(w.lens_lo, w.n_k), w.n_k, seeds[3])
+    if device != "cpu":
+        q, k, v = q.to(device), k.to(device), v.to(device)
+        lens = None if lens is None else lens.to(device)
+    return q, k, v, lens
+
+
+def flops(w: Workload, key_lens=None) -> float:
+    """Nominal FLOPs of one forward pass: 4*B*h*n_q*n_k*d (two contractions of
+    2*n_q*n_k*d each), halved for the causal mask."""
+    f = 4.0 * w.B * w.h * w.n_q * w.n_k * w.d
+    if w.mask == MASK_CAUSAL:
+        f *= 0.5
+    return f
+
+
+def algorithmic_flops(w: Workload, key_lens=None) -> float:
+    """FLOPs over the connections the mask allows: causal counts the exact
+    triangle, key padding counts sum_b L_b keys per query."""
+    if w.mask == MASK_CAUSAL:
+        n = min(w.n_q, w.n_k)
+        pairs = n * (n + 1) / 2 + max(0, w.n_q - n) * w.n_k
+        return 4.0 * w.B * w.h * pairs * w.d
+    if w.mask == MASK_KEY_PADDING:
+        lens = np.asarray(key_lens.cpu() if hasattr(key_lens, "cpu") else key_lens)
+        return 4.0 * w.h * w.n_q * float(np.minimum(lens, w.n_k).sum()) * w.d
+    return flops(w)
+
+
+def hbm_bytes(w: Workload) -> float:
+    """Compulsory HBM bytes of one forward pass: Q, K, V read once, O written
+    once, LSE (float32) written once; the n_q x n_k scores never leave the chip."""
+    es = 2 if w.dtype == "bf16" else 4
+    qo = 2 * w.B * w.h * w.n_q * w.d * es
+    kv = 2 * w.B * w.h * w.n_k * w.d * es
+    return float(qo + kv + 4 * w.B * w.h * w.n_q)
