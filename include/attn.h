@@ -1,0 +1,139 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) multi-head scaled dot-product
+ * attention forward library (libattn_gb300.so).
+ *
+ * The operation (eq. (1) of "Attention Is All You Need", section 3.2.1, as
+ * restated on every page read for this library; the masks of section 3.2.3):
+ *
+ *     O[b,h] = softmax(Q[b,h] K[b,h]^T * scale + M) V[b,h]
+ *     LSE[b,h,i] = ln sum_j exp(scale * q_i.k_j + M_ij)
+ *
+ * for every batch entry b and head h, with M_ij = -inf on forbidden
+ * connections and 0 elsewhere:
+ *   ATTN_MASK_NONE         encoder self-attention: every query sees every key;
+ *   ATTN_MASK_CAUSAL       decoder masked self-attention: query i sees keys
+ *                          j <= i (itself included), top-left aligned when
+ *                          n_q != n_k;
+ *   ATTN_MASK_KEY_PADDING  encoder-decoder attention over padded sequences:
+ *                          query rows of batch entry b see keys j < key_lens[b].
+ * A query row with no visible key gets O = 0 and LSE = -inf.  The usual
+ * scale is 1/sqrt(d_k); it is an argument so that the caller states it.
+ *
+ * Layout (all entry points): contiguous [B, h, n, d] tensors, d innermost;
+ * Q [B,h,n_q,d_k], K [B,h,n_k,d_k], V [B,h,n_k,d_v], O [B,h,n_q,d_v] with
+ * d_v = d_k, LSE [B,h,n_q] float32.
+ *
+ * Ownership and execution: every pointer argument is a device pointer owned
+ * by the caller; the library reads q, k, v, key_lens and writes o and lse
+ * only, never frees caller memory, and allocates no device memory.  Calls
+ * are asynchronous on `stream` (NULL = the legacy default stream): argument
+ * checks happen on the host before anything is enqueued; errors found on the
+ * device are reported by attn_check().  No call synchronises the host.
+ * Errors are returned as attn_status codes; nothing is thrown across the ABI.
+ */
+#ifndef ATTN_GB300_H_
+#define ATTN_GB300_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t */
+
+typedef enum {
+  ATTN_MASK_NONE = 0,
+  ATTN_MASK_CAUSAL = 1,
+  ATTN_MASK_KEY_PADDING = 2
+} attn_mask_kind;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = -1, /* null/misaligned pointer, size < 1, bad mask or scale */
+  ATTN_ERR_UNSUPPORTED = -2, /* head size or device this build does not cover */
+  ATTN_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed, see attn_last_cuda_error */
+  ATTN_ERR_TIMEOUT = -4      /* a kernel gave up on a bounded wait (see attn_check) */
+} attn_status;
+
+/*
+ * attn_fwd -- bf16 forward on the tensor cores (tcgen05 + TMEM + TMA).
+ *   q, k, v : const __nv_bfloat16*, layout above, 16-byte aligned.
+ *   o       : __nv_bfloat16* [B,h,n_q,d_k], written (rounded to nearest even).
+ *   lse     : float* [B,h,n_q] or NULL (then not written).
+ *   B, h, n_q, n_k >= 1; d_k must be 64 (other head sizes: ATTN_ERR_UNSUPPORTED).
+ *   scale   : finite and > 0 (normally 1/sqrt(d_k)).
+ *   mask_kind : an attn_mask_kind.
+ *   key_lens  : device int32[B], required for ATTN_MASK_KEY_PADDING, ignored
+ *               otherwise; values are clamped to [0, n_k] on the device.
+ *   stream  : cudaStream_t.
+ * Scores, softmax and the P.V product are computed in fp32 from bf16 inputs;
+ * P is rounded to bf16 before the second product.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+             int n_q, int n_k, int d_k, float scale, int mask_kind, const int* key_lens,
+             struct CUstream_st* stream);
+
+/*
+ * attn_fwd_f32 -- float32 forward on the CUDA cores (fp32 FMA, same
+ * definition, same arguments with float tensors).  d_k in {16, 32, 64, 128}.
+ */
+int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                 int h, int n_q, int n_k, int d_k, float scale, int mask_kind,
+                 const int* key_lens, struct CUstream_st* stream);
+
+/*
+ * attn_check -- synchronise `stream`, then report (and clear) any error a
+ * kernel of this library recorded on the current device since the last check:
+ * ATTN_ERR_TIMEOUT when a bounded wait inside a kernel ran out (the kernel
+ * returned early and its outputs are incomplete), ATTN_ERR_CUDA when the
+ * synchronisation itself failed, else ATTN_OK.
+ */
+int attn_check(struct CUstream_st* stream);
+
+/* Static description of a status code. */
+const char* attn_status_string(int status);
+
+/* The cudaError_t behind the most recent ATTN_ERR_CUDA in this process. */
+int attn_last_cuda_error(void);
+
+/*
+ * attn_set_wait_limit_ns -- wall-clock limit for every bounded wait inside
+ * the kernels launched after this call (default 2e9 ns).  0 restores the
+ * default.  Returns the previous value.
+ */
+uint64_t attn_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t attn_launch_count(void);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics (not part of the attention operation; used by the tests).
+ * ------------------------------------------------------------------------ */
+
+/*
+ * attn_diag_tile -- one CTA runs the two tensor-core products of a single
+ * 128x128 tile exactly as the fused kernel issues them:
+ *   s = q k^T  (q, k: bf16 [128, 64]; s: float [128, 128])
+ *   o = p v    (p: bf16 [128, 128]; v: bf16 [128, 64]; o: float [128, 64])
+ * q, k and v are staged by TMA with 128-byte swizzle, p is written to tensor
+ * memory by the threads, both products accumulate in tensor memory and are
+ * read back with tcgen05.ld.  All pointers are device pointers, 16-byte
+ * aligned.
+ */
+int attn_diag_tile(const void* q, const void* k, const void* p, const void* v, float* s,
+                   float* o, struct CUstream_st* stream);
+
+/*
+ * attn_diag_wait_timeout -- launch a one-thread kernel that waits on an
+ * mbarrier nobody arrives on, bounded by `limit_ns`; it records
+ * ATTN_ERR_TIMEOUT for attn_check() and returns.  Exercises the failure path
+ * of the bounded waits without faulting the GPU.
+ */
+int attn_diag_wait_timeout(uint64_t limit_ns, struct CUstream_st* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H_ */

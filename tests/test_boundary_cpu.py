@@ -1,0 +1,111 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+include/attn.h declares, and rejects bad arguments on the host before any
+CUDA call."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from transformer_head_scaled_gb300 import binding
+from transformer_head_scaled_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return binding.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert sorted(binding.EXPORTS) == _declared_functions()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4):
+        assert binding.status_string(code) not in ("", "unknown status")
+    assert binding.status_string(7) == "unknown status"
+
+
+def test_wait_limit_round_trip(lib):
+    old = binding.set_wait_limit_ns(12345)
+    assert binding.set_wait_limit_ns(old) == 12345
+    assert binding.set_wait_limit_ns(0) == old      # 0 restores the default
+    binding.set_wait_limit_ns(old)
+
+
+# Fake, never-dereferenced device addresses: validation happens first.
+A = 0x10000  # 16-byte aligned
+
+
+def _call(f32=False, q=A, k=A, v=A, o=A, lse=None, B=1, h=1, n_q=8, n_k=8, d=64, scale=0.125,
+          mask=0, lens=None):
+    return binding.attn_fwd_raw(q, k, v, o, lse, B, h, n_q, n_k, d, scale, mask, lens, None, f32=f32)
+
+
+@pytest.mark.parametrize("f32", [False, True])
+def test_invalid_arguments_rejected_on_host(lib, f32):
+    INV = binding.ATTN_ERR_INVALID_ARG
+    assert _call(f32, q=None) == INV
+    assert _call(f32, o=None) == INV
+    assert _call(f32, k=A + 8) == INV            # misaligned
+    assert _call(f32, lse=A + 2) == INV           # misaligned lse
+    for field in ("B", "h", "n_q", "n_k"):
+        assert _call(f32, **{field: 0}) == INV
+        assert _call(f32, **{field: -3}) == INV
+    assert _call(f32, scale=0.0) == INV
+    assert _call(f32, scale=-1.0) == INV
+    assert _call(f32, scale=math.nan) == INV
+    assert _call(f32, scale=math.inf) == INV
+    assert _call(f32, mask=3) == INV
+    assert _call(f32, mask=-1) == INV
+    assert _call(f32, mask=2, lens=None) == INV   # key padding needs lengths
+    assert _call(f32, mask=2, lens=A + 2) == INV
+    assert _call(f32, B=1 << 20, h=1 << 12) == INV  # B*h beyond 2^31
+
+
+def test_unsupported_head_sizes(lib):
+    UNS = binding.ATTN_ERR_UNSUPPORTED
+    for d in (16, 32, 48, 128):
+        assert _call(False, d=d) == UNS
+    for d in (8, 48, 96, 256):
+        assert _call(True, d=d) == UNS
+
+
+def test_diag_entry_points_validate(lib):
+    assert lib.attn_diag_tile(None, A, A, A, A, A, None) == binding.ATTN_ERR_INVALID_ARG
+    assert lib.attn_diag_tile(A, A, A + 4, A, A, A, None) == binding.ATTN_ERR_INVALID_ARG
+    assert lib.attn_diag_wait_timeout(0, None) == binding.ATTN_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        binding.attn_fwd(x, x, x)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No silent fallback: a missing library is an error."""
+    saved = binding._lib
+    binding._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="missing"):
+            binding.load(str(tmp_path / "nope.so"))
+    finally:
+        binding._lib = saved

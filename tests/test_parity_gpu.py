@@ -1,0 +1,238 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Tolerances (computed on the bf16-rounded inputs, as the oracle sees them):
+  bf16 path:  max |O - O_ref| <= 2e-2, mean |O - O_ref| <= 2e-3, |LSE - LSE_ref| <= 1e-3
+  fp32 path:  max |O - O_ref| <= 1e-4, |LSE - LSE_ref| <= 1e-3
+Small cases compare every element; the full-size workloads compare a sample
+of rows (first/last rows of every 128-row tile band plus random rows), each
+computed by the oracle one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from transformer_head_scaled_gb300 import binding, inputs
+from transformer_head_scaled_gb300.inputs import MASK_CAUSAL, MASK_KEY_PADDING, MASK_NONE, Workload
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX, BF16_MEAN, F32_MAX, LSE_TOL = 2e-2, 2e-3, 1e-4, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from transformer_head_scaled_gb300.build import build
+    build()
+    oracle.build()
+    return binding.load()
+
+
+def _run(q, k, v, mask, lens, scale=None):
+    o, lse = binding.attn_fwd(q, k, v, scale=scale, mask=mask, key_lens=lens)
+    binding.check()
+    return o, lse
+
+
+def _compare(o, lse, o_ref, l_ref, f32=False):
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    err = np.abs(o - o_ref)
+    assert np.isfinite(o).all()
+    if f32:
+        assert err.max() <= F32_MAX, f"max abs err {err.max():.3g}"
+    else:
+        assert err.max() <= BF16_MAX, f"max abs err {err.max():.3g}"
+        assert err.mean() <= BF16_MEAN, f"mean abs err {err.mean():.3g}"
+    fin = np.isfinite(l_ref)
+    assert np.array_equal(np.isneginf(lse), np.isneginf(l_ref))
+    if fin.any():
+        lerr = np.abs(lse[fin] - l_ref[fin]).max()
+        assert lerr <= LSE_TOL, f"lse err {lerr:.3g}"
+    return err.max()
+
+
+def _full_case(w: Workload, seeds=(0, 1, 2, 3), lens=None):
+    q, k, v, kl = inputs.make_inputs(w, device="cuda", seeds=seeds)
+    if lens is not None:
+        kl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    o, lse = _run(q, k, v, w.mask, kl, w.scale)
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, w.scale, w.mask, kl)
+    return _compare(o, lse, o_ref, l_ref, f32=w.dtype == "f32")
+
+
+# ------------------------------------------------------------------ building blocks
+
+def test_diag_tile_products():
+    """One 128x128 tile: S = Q K^T (SS MMA, 128B-swizzled TMA tiles) and
+    O = P V (P from tensor memory, V MN-major) match float64 products."""
+    g = torch.Generator().manual_seed(7)
+    q = torch.randn(128, 64, generator=g).to(torch.bfloat16)
+    k = torch.randn(128, 64, generator=g).to(torch.bfloat16)
+    p = torch.rand(128, 128, generator=g).to(torch.bfloat16)
+    v = torch.randn(128, 64, generator=g).to(torch.bfloat16)
+    s, o = binding.diag_tile(q.cuda(), k.cuda(), p.cuda(), v.cuda())
+    binding.check()
+    s_ref = q.double() @ k.double().T
+    o_ref = p.double() @ v.double()
+    np.testing.assert_allclose(s.cpu().double().numpy(), s_ref.numpy(), atol=1e-3, rtol=1e-5)
+    np.testing.assert_allclose(o.cpu().double().numpy(), o_ref.numpy(), atol=1e-3, rtol=1e-5)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait that nothing completes gives up after its limit, the host sees
+    ATTN_ERR_TIMEOUT, and the context stays usable."""
+    binding.diag_wait_timeout(2_000_000)  # 2 ms
+    with pytest.raises(binding.AttnError) as e:
+        binding.check()
+    assert e.value.status == binding.ATTN_ERR_TIMEOUT
+    binding.check()  # cleared
+    _full_case(Workload("after", 1, 2, 130, 130, 64, MASK_NONE, "bf16"))
+
+
+# ------------------------------------------------------------------ fp32 path
+
+def test_tiny_workload_fp32():
+    assert _full_case(inputs.WORKLOADS["tiny"]) <= F32_MAX
+
+
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+def test_fp32_masks_and_head_sizes(mask, d):
+    w = Workload("f32", 2, 3, 77, 77 if mask == MASK_CAUSAL else 93, d, mask, "f32")
+    _full_case(w, lens=[50, 1] if mask == MASK_KEY_PADDING else None)
+
+
+# ------------------------------------------------------------------ bf16 tensor-core path
+
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING])
+@pytest.mark.parametrize("shape", [(2, 3, 300, 333), (1, 2, 512, 512), (3, 1, 257, 129),
+                                   (1, 1, 1, 1), (2, 2, 1000, 700), (1, 4, 128, 128)])
+def test_bf16_parity_small(mask, shape):
+    B, h, n_q, n_k = shape
+    if mask == MASK_CAUSAL:
+        n_k = n_q
+    lens = None
+    if mask == MASK_KEY_PADDING:
+        lens = [max(1, (n_k * (b + 1)) // (B + 1)) for b in range(B)]
+    _full_case(Workload("s", B, h, n_q, n_k, 64, mask, "bf16"), lens=lens)
+
+
+def test_bf16_key_length_boundaries():
+    """Tile-boundary key lengths, including 0 (no visible key: O = 0, lse = -inf)."""
+    lens = [0, 1, 63, 64, 65, 127, 128, 129, 255, 256, 257, 383, 384, 385, 511, 512]
+    _full_case(Workload("kb", len(lens), 2, 200, 512, 64, MASK_KEY_PADDING, "bf16"), lens=lens)
+
+
+def test_bf16_causal_rectangular():
+    """Causal with n_q != n_k is top-left aligned (query i sees keys j <= i)."""
+    _full_case(Workload("cr", 2, 2, 600, 300, 64, MASK_CAUSAL, "bf16"))
+    _full_case(Workload("cr2", 2, 2, 200, 700, 64, MASK_CAUSAL, "bf16"))
+
+
+def test_bf16_scale_argument():
+    w = Workload("sc", 1, 2, 256, 384, 64, MASK_NONE, "bf16")
+    q, k, v, _ = inputs.make_inputs(w, device="cuda")
+    for scale in (0.05, 0.125, 0.5):
+        o, lse = _run(q, k, v, MASK_NONE, None, scale)
+        o_ref, l_ref = oracle.attn_fwd(q, k, v, scale, MASK_NONE)
+        _compare(o, lse, o_ref, l_ref)
+
+
+def test_bf16_large_scores_stay_finite():
+    """Scores far from zero (|s| ~ 30..60): the running max keeps exp2 in range."""
+    w = Workload("big_s", 1, 2, 256, 1024, 64, MASK_NONE, "bf16")
+    q, k, v, _ = inputs.make_inputs(w, device="cuda")
+    q = (q.float() * 4).to(torch.bfloat16)
+    o, lse = _run(q, k, v, MASK_NONE, None, w.scale)
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, w.scale, MASK_NONE)
+    _compare(o, lse, o_ref, l_ref)
+
+
+# ------------------------------------------------------------------ invariants on the GPU
+
+def test_constant_values_and_causal_first_row():
+    w = Workload("inv", 2, 2, 384, 384, 64, MASK_CAUSAL, "bf16")
+    q, k, v, _ = inputs.make_inputs(w, device="cuda")
+    row = v[:, :, :1].clone()
+    vc = row.expand_as(v).contiguous()
+    for mask in (MASK_NONE, MASK_CAUSAL):
+        o, _ = _run(q, k, vc, mask, None, w.scale)
+        assert torch.allclose(o.float(), row.float().expand_as(o), atol=1e-2)
+    o, lse = _run(q, k, v, MASK_CAUSAL, None, w.scale)
+    assert torch.equal(o[:, :, 0], v[:, :, 0])
+    s00 = (q[:, :, 0].double() * k[:, :, 0].double()).sum(-1) * w.scale
+    assert torch.allclose(lse[:, :, 0].double().cpu(), s00.cpu(), atol=1e-3)
+
+
+def test_full_length_padding_equals_no_mask():
+    w = Workload("eq", 3, 2, 300, 333, 64, MASK_NONE, "bf16")
+    q, k, v, _ = inputs.make_inputs(w, device="cuda")
+    lens = torch.full((3,), 333, dtype=torch.int32, device="cuda")
+    o0, l0 = _run(q, k, v, MASK_NONE, None, w.scale)
+    o1, l1 = _run(q, k, v, MASK_KEY_PADDING, lens, w.scale)
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+
+
+def test_heads_independent_and_deterministic():
+    w = Workload("hd", 2, 4, 300, 300, 64, MASK_NONE, "bf16")
+    q, k, v, _ = inputs.make_inputs(w, device="cuda")
+    o, lse = _run(q, k, v, MASK_NONE, None, w.scale)
+    o2, lse2 = _run(q, k, v, MASK_NONE, None, w.scale)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    for b, h in ((0, 0), (1, 3)):
+        oh, lh = _run(q[b:b+1, h:h+1].contiguous(), k[b:b+1, h:h+1].contiguous(),
+                      v[b:b+1, h:h+1].contiguous(), MASK_NONE, None, w.scale)
+        assert torch.equal(oh[0, 0], o[b, h]) and torch.equal(lh[0, 0], lse[b, h])
+
+
+def test_key_permutation_invariance():
+    w = Workload("perm", 1, 2, 256, 512, 64, MASK_NONE, "bf16")
+    q, k, v, _ = inputs.make_inputs(w, device="cuda")
+    perm = torch.randperm(512, generator=torch.Generator().manual_seed(3)).cuda()
+    o, lse = _run(q, k, v, MASK_NONE, None, w.scale)
+    op, lp = _run(q, k[:, :, perm].contiguous(), v[:, :, perm].contiguous(), MASK_NONE, None, w.scale)
+    assert (o.float() - op.float()).abs().max().item() <= 2e-2
+    assert (lse - lp).abs().max().item() <= 1e-3
+
+
+def test_lse_buffer_optional():
+    w = Workload("nolse", 1, 2, 200, 200, 64, MASK_NONE, "bf16")
+    q, k, v, _ = inputs.make_inputs(w, device="cuda")
+    o1, _ = binding.attn_fwd(q, k, v, with_lse=False)
+    o2, _ = binding.attn_fwd(q, k, v)
+    binding.check()
+    assert torch.equal(o1, o2)
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+def _sample_rows(w: Workload, n_random=1024, seed=0):
+    rng = np.random.default_rng(seed)
+    BH = w.B * w.h
+    rows = set()
+    for bh in rng.choice(BH, size=min(BH, 16), replace=False):
+        for r0 in range(0, w.n_q, 128):
+            for r in (r0, min(r0 + 127, w.n_q - 1)):
+                rows.add(int(bh) * w.n_q + r)
+    rows.update(int(x) for x in rng.integers(0, BH * w.n_q, size=n_random))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["base_enc", "base_dec", "encdec", "big", "big_causal"])
+def test_full_size_workloads_sampled(name):
+    """The workloads the benchmark times, in the same launch configuration,
+    checked on sampled rows computed one by one by the oracle."""
+    w = inputs.WORKLOADS[name]
+    q, k, v, kl = inputs.make_inputs(w, device="cuda")
+    o, lse = _run(q, k, v, w.mask, kl, w.scale)
+    rows = _sample_rows(w, n_random=512 if name.startswith("big") else 2048)
+    o_ref, l_ref = oracle.attn_rows(q, k, v, rows, w.scale, w.mask, kl)
+    o_s = o.reshape(-1, w.d)[torch.from_numpy(rows).cuda()]
+    l_s = lse.reshape(-1)[torch.from_numpy(rows).cuda()]
+    _compare(o_s, l_s, o_ref, l_ref)
+    assert torch.isfinite(o.float()).all()

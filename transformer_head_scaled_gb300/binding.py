@@ -1,0 +1,190 @@
+"""ctypes binding of the C ABI in ``include/attn.h``.
+
+Argument marshalling only: every step of the attention runs in the CUDA
+library.  PyTorch is used for device buffers and streams.  The library must
+have been built (``transformer_head_scaled_gb300.build.build()``); if it is
+missing, :func:`load` raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from .inputs import MASK_CAUSAL, MASK_KEY_PADDING, MASK_NONE  # noqa: F401
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build",
+                        "libattn_gb300.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_CUDA = -3
+ATTN_ERR_TIMEOUT = -4
+
+# Every entry point declared in include/attn.h.
+EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_check", "attn_status_string",
+           "attn_last_cuda_error", "attn_set_wait_limit_ns", "attn_launch_count",
+           "attn_diag_tile", "attn_diag_wait_timeout")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = f"{what}: {status_string(status)} ({status})"
+        if status == ATTN_ERR_CUDA and _lib is not None:
+            msg += f", cudaError {_lib.attn_last_cuda_error()}"
+        super().__init__(msg)
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library (once) and declare the signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library {path} is missing: build it with "
+                "transformer_head_scaled_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        for name in ("attn_fwd", "attn_fwd_f32"):
+            fn = getattr(lib, name)
+            fn.restype = i32
+            fn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, vp]
+        lib.attn_check.restype = i32
+        lib.attn_check.argtypes = [vp]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_status_string.argtypes = [i32]
+        lib.attn_last_cuda_error.restype = i32
+        lib.attn_last_cuda_error.argtypes = []
+        lib.attn_set_wait_limit_ns.restype = ctypes.c_uint64
+        lib.attn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.attn_launch_count.restype = ctypes.c_uint64
+        lib.attn_launch_count.argtypes = []
+        lib.attn_diag_tile.restype = i32
+        lib.attn_diag_tile.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        lib.attn_diag_wait_timeout.restype = i32
+        lib.attn_diag_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    if _lib is None:
+        return str(status)
+    return _lib.attn_status_string(int(status)).decode()
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def attn_fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, n_k, d_k, scale, mask_kind,
+                 key_lens_ptr, stream_ptr, f32: bool = False) -> int:
+    """The C call itself, on raw device pointers; returns the status code."""
+    lib = load()
+    fn = lib.attn_fwd_f32 if f32 else lib.attn_fwd
+    return fn(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, n_k, d_k, float(scale),
+              mask_kind, key_lens_ptr, stream_ptr)
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+             mask: int = MASK_NONE, key_lens: torch.Tensor | None = None,
+             out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+             with_lse: bool = True, stream=None):
+    """O = softmax(Q K^T * scale + M) V on the GPU, q/k/v [B, h, n, d] CUDA tensors.
+
+    bf16 inputs run on the tensor cores (d = 64), float32 inputs on the CUDA
+    cores.  scale defaults to 1/sqrt(d).  Returns (o, lse); lse is None when
+    with_lse is False and no lse buffer is given.
+    """
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if q.dtype != k.dtype or q.dtype != v.dtype or q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q, k, v must all be bfloat16 or all float32")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, h, n, d]")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    B, h, n_q, d = q.shape
+    n_k = k.shape[2]
+    if tuple(k.shape) != (B, h, n_k, d) or tuple(v.shape) != (B, h, n_k, d):
+        raise ValueError("k and v must be [B, h, n_k, d] with q's B, h, d")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    kl = None
+    if mask == MASK_KEY_PADDING:
+        if key_lens is None:
+            raise ValueError("key padding needs key_lens")
+        kl = key_lens
+        if kl.dtype != torch.int32 or not kl.is_cuda or kl.numel() != B or not kl.is_contiguous():
+            raise ValueError("key_lens must be a contiguous int32 CUDA tensor of B entries")
+    if out is None:
+        out = torch.empty((B, h, n_q, d), dtype=q.dtype, device=q.device)
+    if lse is None and with_lse:
+        lse = torch.empty((B, h, n_q), dtype=torch.float32, device=q.device)
+    rc = attn_fwd_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, h, n_q, n_k, d, scale,
+                      int(mask), _ptr(kl), _stream_ptr(stream), f32=q.dtype == torch.float32)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_f32(q, k, v, **kw):
+    """Float32 path (same as attn_fwd with float32 tensors)."""
+    if q.dtype != torch.float32:
+        raise ValueError("attn_fwd_f32 takes float32 tensors")
+    return attn_fwd(q, k, v, **kw)
+
+
+def check(stream=None) -> None:
+    """Synchronise and raise if a kernel recorded an error (bounded wait ran out)."""
+    rc = load().attn_check(_stream_ptr(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_check")
+
+
+def set_wait_limit_ns(limit_ns: int) -> int:
+    return int(load().attn_set_wait_limit_ns(int(limit_ns)))
+
+
+def launch_count() -> int:
+    return int(load().attn_launch_count())
+
+
+def diag_tile(q, k, p, v, stream=None):
+    """Single-tile tensor-core products (see attn_diag_tile in include/attn.h).
+
+    q, k: bf16 [128, 64]; p: bf16 [128, 128]; v: bf16 [128, 64].
+    Returns (s = q k^T float32 [128,128], o = p v float32 [128, 64]).
+    """
+    for t, shp in ((q, (128, 64)), (k, (128, 64)), (p, (128, 128)), (v, (128, 64))):
+        if tuple(t.shape) != shp or t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"diag_tile: expected contiguous bf16 CUDA {shp}")
+    s = torch.empty((128, 128), dtype=torch.float32, device=q.device)
+    o = torch.empty((128, 64), dtype=torch.float32, device=q.device)
+    rc = load().attn_diag_tile(_ptr(q), _ptr(k), _ptr(p), _ptr(v), _ptr(s), _ptr(o),
+                               _stream_ptr(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_diag_tile")
+    return s, o
+
+
+def diag_wait_timeout(limit_ns: int, stream=None) -> None:
+    rc = load().attn_diag_wait_timeout(int(limit_ns), _stream_ptr(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_diag_wait_timeout")

@@ -1,0 +1,255 @@
+// attn_api.cu -- the library's C ABI (declared in include/attn.h): argument
+// checks, per-device set-up, TMA tensor-map encoding and kernel dispatch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_internal.cuh"
+
+namespace attn {
+namespace {
+
+// Errors a kernel finds (a bounded wait that ran out) are recorded here, one
+// word per device, and read back by attn_check().
+__device__ int g_status;
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultLimitNs = 2000000000ull;
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int num_sms = 0;
+  int* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<uint64_t> g_limit_ns{kDefaultLimitNs};
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_last_cuda_error{0};
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error.store(static_cast<int>(e));
+  return ATTN_ERR_CUDA;
+}
+
+// Per-device set-up on first use: SM count, architecture check, address of
+// the status word, the driver's tensor-map encoder.
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    di.supported = (major == 10 && minor == 3);  // the kernels are built for sm_103a only
+    di.num_sms = sms;
+    if (di.supported) {
+      void* addr = nullptr;
+      if ((e = cudaGetSymbolAddress(&addr, g_status)) != cudaSuccess) return cuda_fail(e);
+      di.status = static_cast<int*>(addr);
+    }
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q);
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cuda_fail(cudaErrorNotSupported);
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    di.ready = true;
+  }
+  if (!di.supported) return ATTN_ERR_UNSUPPORTED;
+  *out = &di;
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 int B, int h, int n_q, int n_k, int d_k, float scale, int mask_kind,
+                 const int* key_lens, size_t elem) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || h < 1 || n_q < 1 || n_k < 1 || d_k < 1) return ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (mask_kind != ATTN_MASK_NONE && mask_kind != ATTN_MASK_CAUSAL &&
+      mask_kind != ATTN_MASK_KEY_PADDING)
+    return ATTN_ERR_INVALID_ARG;
+  if (mask_kind == ATTN_MASK_KEY_PADDING &&
+      (key_lens == nullptr || (reinterpret_cast<uintptr_t>(key_lens) & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  // Index arithmetic: B*h fits a TMA coordinate and a grid; every tensor
+  // stays below 2^40 bytes (the TMA stride limit).
+  const long long bh = static_cast<long long>(B) * h;
+  if (bh > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  const long long n = n_q > n_k ? n_q : n_k;
+  if (bh * n * d_k * static_cast<long long>(elem) >= (1LL << 40)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+// (d, n, B*H) bf16 view with a (64, rows, 1) box and 128-byte swizzle.
+int encode_3d(CUtensorMap* map, const void* base, int d, int n, long long bh, int box_rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
+                        static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(n)};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
+}
+
+int encode_2d(CUtensorMap* map, const void* base) {
+  cuuint64_t dims[2] = {64, 128};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
+}
+
+LaunchCtx make_ctx(const DeviceInfo& di, cudaStream_t stream) {
+  LaunchCtx ctx;
+  ctx.num_sms = di.num_sms;
+  ctx.limit_ns = g_limit_ns.load();
+  ctx.status = di.status;
+  ctx.stream = stream;
+  return ctx;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+             int n_q, int n_k, int d_k, float scale, int mask_kind, const int* key_lens,
+             struct CUstream_st* stream) {
+  int rc = check_common(q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, mask_kind, key_lens, 2);
+  if (rc != ATTN_OK) return rc;
+  if (d_k != 64) return ATTN_ERR_UNSUPPORTED;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di)) != ATTN_OK) return rc;
+  const long long bh = static_cast<long long>(B) * h;
+  CUtensorMap tmq, tmk, tmv;
+  if ((rc = encode_3d(&tmq, q, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&tmk, k, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&tmv, v, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
+  Problem pb{q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, mask_kind,
+             mask_kind == ATTN_MASK_KEY_PADDING ? key_lens : nullptr};
+  cudaError_t e = launch_fwd_tc(pb, tmq, tmk, tmv, make_ctx(*di, stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
+int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                 int h, int n_q, int n_k, int d_k, float scale, int mask_kind,
+                 const int* key_lens, struct CUstream_st* stream) {
+  int rc = check_common(q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, mask_kind, key_lens, 4);
+  if (rc != ATTN_OK) return rc;
+  if (d_k != 16 && d_k != 32 && d_k != 64 && d_k != 128) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * h > 65535) return ATTN_ERR_UNSUPPORTED;  // grid.y
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di)) != ATTN_OK) return rc;
+  Problem pb{q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, mask_kind,
+             mask_kind == ATTN_MASK_KEY_PADDING ? key_lens : nullptr};
+  cudaError_t e = launch_fwd_f32(pb, make_ctx(*di, stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
+int attn_check(struct CUstream_st* stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  DeviceInfo* di = nullptr;
+  int rc = device_info(&di);
+  if (rc != ATTN_OK) return rc;
+  int status = 0;
+  if ((e = cudaMemcpyFromSymbol(&status, g_status, sizeof(int))) != cudaSuccess) return cuda_fail(e);
+  if (status != kDevOk) {
+    const int zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int))) != cudaSuccess) return cuda_fail(e);
+    return ATTN_ERR_TIMEOUT;
+  }
+  return ATTN_OK;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported head size or device";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "a bounded wait inside a kernel timed out";
+    default: return "unknown status";
+  }
+}
+
+int attn_last_cuda_error(void) { return g_last_cuda_error.load(); }
+
+uint64_t attn_set_wait_limit_ns(uint64_t limit_ns) {
+  return g_limit_ns.exchange(limit_ns == 0 ? kDefaultLimitNs : limit_ns);
+}
+
+uint64_t attn_launch_count(void) { return g_launches.load(); }
+
+int attn_diag_tile(const void* q, const void* k, const void* p, const void* v, float* s,
+                   float* o, struct CUstream_st* stream) {
+  if (!q || !k || !p || !v || !s || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(p) || !aligned16(v) || !aligned16(s) ||
+      !aligned16(o))
+    return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  int rc = device_info(&di);
+  if (rc != ATTN_OK) return rc;
+  CUtensorMap tmq, tmk, tmv;
+  if ((rc = encode_2d(&tmq, q)) != ATTN_OK) return rc;
+  if ((rc = encode_2d(&tmk, k)) != ATTN_OK) return rc;
+  if ((rc = encode_2d(&tmv, v)) != ATTN_OK) return rc;
+  cudaError_t e = launch_diag_tile(tmq, tmk, tmv, p, s, o, make_ctx(*di, stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
+int attn_diag_wait_timeout(uint64_t limit_ns, struct CUstream_st* stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  int rc = device_info(&di);
+  if (rc != ATTN_OK) return rc;
+  cudaError_t e = launch_diag_wait_timeout(limit_ns, make_ctx(*di, stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,512 @@
+// attn_fwd_tc.cu -- fused multi-head scaled dot-product attention forward
+// for sm_103a: TMA stages Q/K/V tiles in shared memory, tcgen05 MMAs compute
+// S = Q K^T and O += P V into tensor memory, and an exp2 online softmax keeps
+// the n_q x n_k score matrix on chip.
+//
+// What is computed is eq. (1) of "Attention Is All You Need" (section 3.2.1),
+// softmax(Q K^T / sqrt(d_k)) V per head, with the forbidden connections of
+// section 3.2.3 set to -inf before the softmax (causal: key j > query i;
+// key padding: key j >= key_lens[b]).  The streaming (online) softmax is an
+// exact re-association of the row softmax: the pages name it only through
+// FlashAttention ("32 Transformer": exact attention without materialising
+// the N x N matrix).
+//
+// Structure (one persistent CTA per SM, 320 threads):
+//   warps 0-3  softmax of Q tile 0 (rows 0-127 of a 256-row work item),
+//              one thread per row = one tensor-memory lane;
+//   warps 4-7  softmax of Q tile 1 (rows 128-255);
+//   warp  8    TMA producer (Q tiles per item, a 3-deep K and V ring);
+//   warp  9    tensor-memory owner and single-thread MMA issuer.
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   S0 [0,128)  S1 [128,256)  O0 [256,320)  O1 [320,384)  P0 [384,448)  P1 [448,512)
+// The MMA issue order per KV tile j is  PV0(j-1), S0(j), PV1(j-1), S1(j):
+// while softmax 0 works on S0(j) the tensor pipe computes stage 1, and the
+// reverse, so the exp work of one Q tile overlaps the MMAs of the other.
+// Every wait is bounded; on timeout the kernel records kDevTimeout, all roles
+// drain and the CTA returns.
+#include <cuda_bf16.h>
+
+#include "attn_internal.cuh"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;      // query rows per Q tile (= tensor-memory lanes)
+constexpr int QT = 2;        // Q tiles per work item
+constexpr int ROWS = BM * QT;
+constexpr int BN = 128;      // keys per K/V tile
+constexpr int D = 64;        // head size
+constexpr int STAGES = 3;    // K/V ring depth
+constexpr uint32_t TILE_BYTES = BM * D * 2;  // a Q, K or V tile: 16 KB
+constexpr int LOAD_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr int NUM_THREADS = 320;
+constexpr uint32_t TMEM_COLS = 512;
+// Keep a stale running max until the row max has grown by more than 2^8:
+// P = 2^(x - m) then stays <= 256, exact in bf16's range and harmless for
+// the fp32 accumulators, and O/l is unchanged because both use the same m.
+constexpr float RESCALE_THRESHOLD = 8.0f;
+constexpr float LN2 = 0.693147180559945309f;
+
+__host__ __device__ constexpr uint32_t col_s(int s) { return 128u * s; }
+__host__ __device__ constexpr uint32_t col_o(int s) { return 256u + 64u * s; }
+__host__ __device__ constexpr uint32_t col_p(int s) { return 384u + 64u * s; }
+
+struct __align__(1024) Smem {
+  uint8_t q[QT][TILE_BYTES];
+  uint8_t k[STAGES][TILE_BYTES];
+  uint8_t v[STAGES][TILE_BYTES];
+  uint64_t q_full[QT], q_empty[QT];
+  uint64_t k_full[STAGES], k_empty[STAGES];
+  uint64_t v_full[STAGES], v_empty[STAGES];
+  uint64_t s_full[QT], p_full[QT], o_full[QT];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Params {
+  __nv_bfloat16* o;
+  float* lse;
+  const int* key_lens;
+  int H, n_q, n_k, BH;
+  int mask;
+  int num_qblocks;
+  int num_items;
+  float scale_log2;  // scale * log2(e): exp(scale*s) = 2^(s*scale_log2)
+  uint64_t limit_ns;
+  int* status;
+};
+
+// A work item: 256 query rows of one (b, h).  n[s] = K/V tiles Q tile s
+// visits (0 when the tile lies past n_q).
+struct Item {
+  int bh, qb;
+  int key_limit;
+  int n[QT];
+};
+
+__device__ __forceinline__ Item decode_item(const Params& p, int t) {
+  Item it;
+  if (p.mask == kMaskCausal) {
+    // heaviest row blocks first (longest-processing-time order)
+    it.qb = p.num_qblocks - 1 - t / p.BH;
+    it.bh = t % p.BH;
+  } else {
+    // the row blocks of one head back to back, so K/V stay hot in L2
+    it.qb = t % p.num_qblocks;
+    it.bh = t / p.num_qblocks;
+  }
+  int limit = p.n_k;
+  if (p.mask == kMaskKeyPadding) {
+    const int L = __ldg(p.key_lens + it.bh / p.H);
+    limit = min(max(L, 0), p.n_k);
+  }
+  it.key_limit = limit;
+  const int tiles = (limit + BN - 1) / BN;
+#pragma unroll
+  for (int s = 0; s < QT; ++s) {
+    const int row0 = it.qb * ROWS + s * BM;
+    int n = tiles;
+    if (row0 >= p.n_q) {
+      n = 0;
+    } else if (p.mask == kMaskCausal) {
+      const int last_row = min(row0 + BM - 1, p.n_q - 1);
+      n = min(tiles, last_row / BN + 1);
+    }
+    it.n[s] = n;
+  }
+  return it;
+}
+
+__device__ __forceinline__ void record_timeout(const Params& p, Smem& sm) {
+  atomicCAS(p.status, kDevOk, kDevTimeout);
+  *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq,
+                       const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const volatile int* abort = &sm.abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < QT; ++s) {
+      mbar_init(smem_u32(&sm.q_full[s]), 1);
+      mbar_init(smem_u32(&sm.q_empty[s]), 1);
+      mbar_init(smem_u32(&sm.s_full[s]), 1);
+      mbar_init(smem_u32(&sm.p_full[s]), BM);
+      mbar_init(smem_u32(&sm.o_full[s]), 1);
+    }
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_u32(&sm.k_full[i]), 1);
+      mbar_init(smem_u32(&sm.k_empty[i]), 1);
+      mbar_init(smem_u32(&sm.v_full[i]), 1);
+      mbar_init(smem_u32(&sm.v_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&sm.drain), 1);
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == LOAD_WARP && lane == 0) {
+    prefetch_tmap(&tmq);
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(smem_u32(&sm.tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == LOAD_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t kv = 0;
+      uint32_t items = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x, ++items) {
+        const Item it = decode_item(p, t);
+        const int nmax = max(it.n[0], it.n[1]);
+        for (int s = 0; s < QT && ok; ++s) {
+          ok = mbar_wait(smem_u32(&sm.q_empty[s]), (items & 1) ^ 1, p.limit_ns, abort);
+          if (!ok) break;
+          const uint32_t bar = smem_u32(&sm.q_full[s]);
+          if (it.n[s] > 0) {
+            mbar_arrive_expect_tx(bar, TILE_BYTES);
+            tma_load_3d(smem_u32(sm.q[s]), &tmq, bar, 0, it.qb * ROWS + s * BM, it.bh);
+          } else {
+            mbar_arrive(bar);
+          }
+        }
+        for (int j = 0; j < nmax && ok; ++j, ++kv) {
+          const uint32_t slot = kv % STAGES, ph = (kv / STAGES) & 1;
+          ok = mbar_wait(smem_u32(&sm.k_empty[slot]), ph ^ 1, p.limit_ns, abort);
+          if (!ok) break;
+          mbar_arrive_expect_tx(smem_u32(&sm.k_full[slot]), TILE_BYTES);
+          tma_load_3d(smem_u32(sm.k[slot]), &tmk, smem_u32(&sm.k_full[slot]), 0, j * BN, it.bh);
+          ok = mbar_wait(smem_u32(&sm.v_empty[slot]), ph ^ 1, p.limit_ns, abort);
+          if (!ok) break;
+          mbar_arrive_expect_tx(smem_u32(&sm.v_full[slot]), TILE_BYTES);
+          tma_load_3d(smem_u32(sm.v[slot]), &tmv, smem_u32(&sm.v_full[slot]), 0, j * BN, it.bh);
+        }
+      }
+      if (!ok) {
+        record_timeout(p, sm);
+        // let the copies already issued land before the CTA's shared memory
+        // goes away: wait (bounded, ignoring the abort flag) for the last
+        // phase armed on every full barrier.
+        const int never = 0;
+        for (uint32_t i = 0; i < STAGES; ++i) {
+          const uint32_t uses = kv / STAGES + (i < kv % STAGES ? 1u : 0u);
+          if (uses > 0) {
+            mbar_wait(smem_u32(&sm.k_full[i]), (uses - 1) & 1, p.limit_ns, &never);
+            mbar_wait(smem_u32(&sm.v_full[i]), (uses - 1) & 1, p.limit_ns, &never);
+          }
+        }
+        for (int s = 0; s < QT; ++s)
+          if (items > 0) mbar_wait(smem_u32(&sm.q_full[s]), (items - 1) & 1, p.limit_ns, &never);
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
+      constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, false, true);    // V is MN-major
+      uint32_t kv = 0;
+      uint32_t items = 0;
+      uint32_t pcnt[QT] = {0, 0};
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x, ++items) {
+        const Item it = decode_item(p, t);
+        const int nmax = max(it.n[0], it.n[1]);
+        for (int s = 0; s < QT && ok; ++s)
+          ok = mbar_wait(smem_u32(&sm.q_full[s]), items & 1, p.limit_ns, abort);
+        if (!ok) break;
+        tc_fence_after();
+
+        uint32_t prev_slot = 0, prev_ph = 0;
+        // O_s += P_s V_(j-1); the first product of an item overwrites O_s.
+        auto issue_pv = [&](int s, int j_prev, uint32_t vslot) {
+          const uint32_t vbase = smem_u32(sm.v[vslot]);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            // B = V rows kk*16 .. kk*16+15 (K dim = keys), MN-major, 128B swizzle:
+            // 8-row groups 1024 B apart (SBO).  N = 64 is a single 128-byte swizzle
+            // atom, so the MN-direction stride (LBO) is never applied; it is set to
+            // the same 1024 B so that no reading of the fields leaves the tile.
+            const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, 1024, 1024);
+            mma_ts(tmem + col_o(s), tmem + col_p(s) + kk * 8, bdesc, IDESC_O,
+                   (j_prev > 0 || kk > 0) ? 1u : 0u);
+          }
+        };
+        for (int j = 0; j < nmax && ok; ++j, ++kv) {
+          const uint32_t slot = kv % STAGES, ph = (kv / STAGES) & 1;
+          ok = mbar_wait(smem_u32(&sm.k_full[slot]), ph, p.limit_ns, abort);
+          if (!ok) break;
+          tc_fence_after();
+          bool v_ready = false;
+          for (int s = 0; s < QT && ok; ++s) {
+            if (j > 0 && j <= it.n[s]) {
+              if (!v_ready) {
+                ok = mbar_wait(smem_u32(&sm.v_full[prev_slot]), prev_ph, p.limit_ns, abort);
+                if (!ok) break;
+                v_ready = true;
+              }
+              ok = mbar_wait(smem_u32(&sm.p_full[s]), pcnt[s] & 1, p.limit_ns, abort);
+              if (!ok) break;
+              ++pcnt[s];
+              tc_fence_after();
+              issue_pv(s, j - 1, prev_slot);
+              if (j == it.n[s]) tc_commit(smem_u32(&sm.o_full[s]));
+            }
+            if (j < it.n[s]) {
+              const uint32_t qbase = smem_u32(sm.q[s]);
+              const uint32_t kbase = smem_u32(sm.k[slot]);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                // K-major, 128B swizzle: advance 32 bytes per 16-element K step
+                // inside the swizzle row; 8-row groups 1024 B apart.
+                const uint64_t adesc = sdesc_sw128(qbase + kk * 32, 16, 1024);
+                const uint64_t bdesc = sdesc_sw128(kbase + kk * 32, 16, 1024);
+                mma_ss(tmem + col_s(s), adesc, bdesc, IDESC_S, kk > 0 ? 1u : 0u);
+              }
+              tc_commit(smem_u32(&sm.s_full[s]));
+            }
+          }
+          if (!ok) break;
+          tc_commit(smem_u32(&sm.k_empty[slot]));
+          if (j > 0) tc_commit(smem_u32(&sm.v_empty[prev_slot]));
+          prev_slot = slot;
+          prev_ph = ph;
+        }
+        if (!ok) break;
+        for (int s = 0; s < QT; ++s) tc_commit(smem_u32(&sm.q_empty[s]));
+        if (nmax > 0) {
+          bool v_ready = false;
+          for (int s = 0; s < QT && ok; ++s) {
+            if (it.n[s] != nmax) continue;
+            if (!v_ready) {
+              ok = mbar_wait(smem_u32(&sm.v_full[prev_slot]), prev_ph, p.limit_ns, abort);
+              if (!ok) break;
+              v_ready = true;
+            }
+            ok = mbar_wait(smem_u32(&sm.p_full[s]), pcnt[s] & 1, p.limit_ns, abort);
+            if (!ok) break;
+            ++pcnt[s];
+            tc_fence_after();
+            issue_pv(s, nmax - 1, prev_slot);
+            tc_commit(smem_u32(&sm.o_full[s]));
+          }
+          if (!ok) break;
+          tc_commit(smem_u32(&sm.v_empty[prev_slot]));
+        }
+      }
+      if (!ok) record_timeout(p, sm);
+      // every MMA issued by this thread completes before tensor memory is freed
+      tc_commit(smem_u32(&sm.drain));
+      const int never = 0;
+      mbar_wait(smem_u32(&sm.drain), 0, p.limit_ns, &never);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int s = warp >> 2;
+    const int quarter = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + col_s(s);
+    const uint32_t tO = tmem + lane_off + col_o(s);
+    const uint32_t tP = tmem + lane_off + col_p(s);
+    const bool causal = p.mask == kMaskCausal;
+    const float c = p.scale_log2;
+    uint32_t scnt = 0, ocnt = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
+      const Item it = decode_item(p, t);
+      const int row0 = it.qb * ROWS + s * BM;
+      const int row = row0 + quarter * 32 + lane;
+      float m = -INFINITY;  // running max of scale*log2(e)*score (possibly stale)
+      float l = 0.f;        // running sum of 2^(x - m)
+      for (int j = 0; j < it.n[s]; ++j) {
+        ok = mbar_wait(smem_u32(&sm.s_full[s]), scnt & 1, p.limit_ns, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ++scnt;
+        tc_fence_after();
+        uint32_t r[4][32];
+        tmem_ld32(tS + 0, r[0]);
+        tmem_ld32(tS + 32, r[1]);
+        tmem_ld32(tS + 64, r[2]);
+        tmem_ld32(tS + 96, r[3]);
+        tmem_ld_wait(r[0]);
+        reg_fence(r[1]);
+        reg_fence(r[2]);
+        reg_fence(r[3]);
+
+        const int kbase = j * BN;
+        if (kbase + BN > it.key_limit || (causal && kbase + BN - 1 > row0)) {
+          int lim = it.key_limit - kbase;  // columns >= lim are forbidden
+          if (causal) lim = min(lim, row - kbase + 1);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (q4 * 32 + i >= lim) r[q4][i] = __float_as_uint(-INFINITY);
+        }
+
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[q4][i]));
+        const float rowmax =
+            fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float mt = rowmax * c;
+
+        bool rescale_o = false;
+        float alpha = 1.f;
+        if (mt > m + RESCALE_THRESHOLD) {
+          alpha = ex2(m - mt);  // 0 when m = -inf
+          l *= alpha;
+          rescale_o = j > 0;
+          m = mt;
+        }
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          // O_s is stable here: s_full of tile j is committed after PV(j-1).
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tO, o0);
+          tmem_ld32(tO + 32, o1);
+          tmem_ld_wait(o0);
+          reg_fence(o1);
+          const float a = rescale_o ? alpha : 1.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            o0[i] = __float_as_uint(__uint_as_float(o0[i]) * a);
+            o1[i] = __float_as_uint(__uint_as_float(o1[i]) * a);
+          }
+          tmem_st32(tO, o0);
+          tmem_st32(tO + 32, o1);
+        }
+
+        const float neg_m = (m == -INFINITY) ? 0.f : -m;
+        float ls[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ls[i] = 0.f;
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(r[q4][i]), c, neg_m));
+            const float p1 = ex2(fmaf(__uint_as_float(r[q4][i + 1]), c, neg_m));
+            ls[(i >> 1) & 7] += p0 + p1;
+            pk[q4 >> 1][(q4 & 1) * 16 + (i >> 1)] = pack_bf16x2(p0, p1);
+          }
+        }
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        tmem_st32(tP, pk[0]);
+        tmem_st32(tP + 32, pk[1]);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.p_full[s]));
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue
+      uint32_t o0[32], o1[32];
+      if (it.n[s] > 0) {
+        ok = mbar_wait(smem_u32(&sm.o_full[s]), ocnt & 1, p.limit_ns, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        ++ocnt;
+        tc_fence_after();
+        tmem_ld32(tO, o0);
+        tmem_ld32(tO + 32, o1);
+        tmem_ld_wait(o0);
+        reg_fence(o1);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0u;
+      }
+      if (row < p.n_q) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(it.bh) * p.n_q + row) * D);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(o0[g * 8 + 0]) * inv, __uint_as_float(o0[g * 8 + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(o0[g * 8 + 2]) * inv, __uint_as_float(o0[g * 8 + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(o0[g * 8 + 4]) * inv, __uint_as_float(o0[g * 8 + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(o0[g * 8 + 6]) * inv, __uint_as_float(o0[g * 8 + 7]) * inv);
+          dst[g] = w;
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(o1[g * 8 + 0]) * inv, __uint_as_float(o1[g * 8 + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(o1[g * 8 + 2]) * inv, __uint_as_float(o1[g * 8 + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(o1[g * 8 + 4]) * inv, __uint_as_float(o1[g * 8 + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(o1[g * 8 + 6]) * inv, __uint_as_float(o1[g * 8 + 7]) * inv);
+          dst[4 + g] = w;
+        }
+        if (p.lse != nullptr)
+          p.lse[static_cast<size_t>(it.bh) * p.n_q + row] =
+              l > 0.f ? (m + __log2f(l)) * LN2 : -INFINITY;
+      }
+    }
+    if (!ok) record_timeout(p, sm);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+size_t fwd_tc_smem_bytes() { return sizeof(Smem) + 1024; }
+
+cudaError_t launch_fwd_tc(const Problem& pb, const CUtensorMap& tmq, const CUtensorMap& tmk,
+                          const CUtensorMap& tmv, const LaunchCtx& ctx) {
+  Params p;
+  p.o = static_cast<__nv_bfloat16*>(pb.o);
+  p.lse = pb.lse;
+  p.key_lens = pb.key_lens;
+  p.H = pb.H;
+  p.n_q = pb.n_q;
+  p.n_k = pb.n_k;
+  p.BH = pb.B * pb.H;
+  p.mask = pb.mask;
+  p.num_qblocks = (pb.n_q + ROWS - 1) / ROWS;
+  p.num_items = p.BH * p.num_qblocks;
+  p.scale_log2 = pb.scale * 1.4426950408889634f;
+  p.limit_ns = ctx.limit_ns;
+  p.status = ctx.status;
+  const size_t smem = fwd_tc_smem_bytes();
+  cudaError_t err = cudaFuncSetAttribute(attn_fwd_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  const int grid = p.num_items < ctx.num_sms ? p.num_items : ctx.num_sms;
+  attn_fwd_tc_kernel<<<grid, NUM_THREADS, smem, ctx.stream>>>(tmq, tmk, tmv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,52 @@
+// attn_internal.cuh -- declarations shared by the library's translation
+// units (host launchers and the status codes the kernels record).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace attn {
+
+enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskKeyPadding = 2 };
+
+// Written (first error wins) into the library's device status word.
+enum DeviceStatus : int { kDevOk = 0, kDevTimeout = 1 };
+
+// One forward problem, device pointers, [B, H, n, d] contiguous.
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, H, n_q, n_k, d;
+  float scale;
+  int mask;
+  const int* key_lens;
+};
+
+// Launch context shared by every launcher.
+struct LaunchCtx {
+  int num_sms;
+  uint64_t limit_ns;  // bounded-wait limit inside kernels
+  int* status;        // device address of the status word
+  cudaStream_t stream;
+};
+
+// tcgen05 bf16 path (d = 64).  The tensor maps describe Q, K, V as 3-D
+// (d, n, B*H) bf16 tensors with a (64, 128, 1) box and 128-byte swizzle.
+cudaError_t launch_fwd_tc(const Problem& pb, const CUtensorMap& tmq, const CUtensorMap& tmk,
+                          const CUtensorMap& tmv, const LaunchCtx& ctx);
+size_t fwd_tc_smem_bytes();
+
+// fp32 SIMT path (d in {16, 32, 64, 128}).
+cudaError_t launch_fwd_f32(const Problem& pb, const LaunchCtx& ctx);
+
+// Diagnostics.  The tensor maps are 2-D (64, 128) bf16, one box each.
+cudaError_t launch_diag_tile(const CUtensorMap& tmq, const CUtensorMap& tmk,
+                             const CUtensorMap& tmv, const void* p, float* s, float* o,
+                             const LaunchCtx& ctx);
+cudaError_t launch_diag_wait_timeout(uint64_t limit_ns, const LaunchCtx& ctx);
+
+}  // namespace attn
