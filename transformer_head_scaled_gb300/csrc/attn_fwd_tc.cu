@@ -11,12 +11,13 @@
 // FlashAttention ("32 Transformer": exact attention without materialising
 // the N x N matrix).
 //
-// Structure (one persistent CTA per SM, 320 threads):
+// Structure (one persistent CTA per SM, 384 threads):
 //   warps 0-3  softmax of Q tile 0 (rows 0-127 of a 256-row work item),
 //              one thread per row = one tensor-memory lane;
 //   warps 4-7  softmax of Q tile 1 (rows 128-255);
 //   warp  8    TMA producer (Q tiles per item, a 3-deep K and V ring);
-//   warp  9    tensor-memory owner and single-thread MMA issuer.
+//   warp  9    tensor-memory owner and single-thread MMA issuer;
+//   warps 10-11 idle (they only complete the producer warpgroup).
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   S0 [0,128)  S1 [128,256)  O0 [256,320)  O1 [320,384)  P0 [384,448)  P1 [448,512)
 // The MMA issue order per KV tile j is  PV0(j-1), S0(j), PV1(j-1), S1(j):
@@ -43,7 +44,14 @@ constexpr int STAGES = 3;    // K/V ring depth
 constexpr uint32_t TILE_BYTES = BM * D * 2;  // a Q, K or V tile: 16 KB
 constexpr int LOAD_WARP = 8;
 constexpr int MMA_WARP = 9;
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 384;  // 3 warpgroups: softmax 0, softmax 1, producer + MMA
+// Launched at 168 registers a thread (65536 / 384, rounded down to a multiple
+// of 8); the producer warpgroup hands registers to the two softmax
+// warpgroups: 2 * 208 + 80 <= 3 * 168.
+constexpr int LAUNCH_REGS = 168;
+constexpr uint32_t SOFTMAX_REGS = 208;
+constexpr uint32_t PRODUCER_REGS = 80;
+static_assert(2 * SOFTMAX_REGS + PRODUCER_REGS <= 3 * LAUNCH_REGS, "register split");
 constexpr uint32_t TMEM_COLS = 512;
 // Keep a stale running max until the row max has grown by more than 2^8:
 // P = 2^(x - m) then stays <= 256, exact in bf16's range and harmless for
@@ -62,7 +70,7 @@ struct __align__(1024) Smem {
   uint64_t q_full[QT], q_empty[QT];
   uint64_t k_full[STAGES], k_empty[STAGES];
   uint64_t v_full[STAGES], v_empty[STAGES];
-  uint64_t s_full[QT], p_full[QT], o_full[QT];
+  uint64_t s_full[QT], s_free[QT], p_full[QT], pv_done[QT];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -143,8 +151,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(smem_u32(&sm.q_full[s]), 1);
       mbar_init(smem_u32(&sm.q_empty[s]), 1);
       mbar_init(smem_u32(&sm.s_full[s]), 1);
+      mbar_init(smem_u32(&sm.s_free[s]), BM);
       mbar_init(smem_u32(&sm.p_full[s]), BM);
-      mbar_init(smem_u32(&sm.o_full[s]), 1);
+      mbar_init(smem_u32(&sm.pv_done[s]), 1);
     }
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(smem_u32(&sm.k_full[i]), 1);
@@ -170,7 +179,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp == LOAD_WARP) {
+  if (warp >= LOAD_WARP) {
+    setmaxnreg_dec<PRODUCER_REGS>();
+   if (warp == LOAD_WARP) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t kv = 0;
@@ -221,97 +232,118 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
+    // Fixed issue order, one round per K/V tile j of an item:
+    //   S0(j), S1(j), PV0(j-1), PV1(j-1)
+    // S_s(j) waits only until softmax s has copied S_s(j-1) into registers
+    // (s_free), so the next scores are computed while the softmax of the
+    // previous tile runs; PV_s(j-1) waits for P_s(j-1) (p_full).  The next
+    // item's S(0) products go before this item's last PV products.
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
       constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, false, true);    // V is MN-major
-      uint32_t kv = 0;
-      uint32_t items = 0;
-      uint32_t pcnt[QT] = {0, 0};
+      uint32_t sc0 = 0, sc1 = 0;  // S products issued per stage (all items)
+      uint32_t pc0 = 0, pc1 = 0;  // PV products issued per stage
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x, ++items) {
-        const Item it = decode_item(p, t);
-        const int nmax = max(it.n[0], it.n[1]);
-        for (int s = 0; s < QT && ok; ++s)
-          ok = mbar_wait(smem_u32(&sm.q_full[s]), items & 1, p.limit_ns, abort);
-        if (!ok) break;
-        tc_fence_after();
 
-        uint32_t prev_slot = 0, prev_ph = 0;
-        // O_s += P_s V_(j-1); the first product of an item overwrites O_s.
-        auto issue_pv = [&](int s, int j_prev, uint32_t vslot) {
-          const uint32_t vbase = smem_u32(sm.v[vslot]);
+      auto wait = [&](uint64_t& bar, uint32_t parity) {
+        if (ok) ok = mbar_wait(smem_u32(&bar), parity, p.limit_ns, abort);
+        return ok;
+      };
+      // S_s(j) for the tile in ring slot g; `last` releases Q tile s.
+      auto issue_s = [&](int s, uint32_t g, bool last) {
+        uint32_t& sc = s == 0 ? sc0 : sc1;
+        if (sc > 0 && !wait(sm.s_free[s], (sc - 1) & 1)) return;
+        tc_fence_after();
+        const uint32_t qbase = smem_u32(sm.q[s]);
+        const uint32_t kbase = smem_u32(sm.k[g % STAGES]);
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            // B = V rows kk*16 .. kk*16+15 (K dim = keys), MN-major, 128B swizzle:
-            // 8-row groups 1024 B apart (SBO).  N = 64 is a single 128-byte swizzle
-            // atom, so the MN-direction stride (LBO) is never applied; it is set to
-            // the same 1024 B so that no reading of the fields leaves the tile.
-            const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, 1024, 1024);
-            mma_ts(tmem + col_o(s), tmem + col_p(s) + kk * 8, bdesc, IDESC_O,
-                   (j_prev > 0 || kk > 0) ? 1u : 0u);
-          }
-        };
-        for (int j = 0; j < nmax && ok; ++j, ++kv) {
-          const uint32_t slot = kv % STAGES, ph = (kv / STAGES) & 1;
-          ok = mbar_wait(smem_u32(&sm.k_full[slot]), ph, p.limit_ns, abort);
-          if (!ok) break;
-          tc_fence_after();
-          bool v_ready = false;
-          for (int s = 0; s < QT && ok; ++s) {
-            if (j > 0 && j <= it.n[s]) {
-              if (!v_ready) {
-                ok = mbar_wait(smem_u32(&sm.v_full[prev_slot]), prev_ph, p.limit_ns, abort);
-                if (!ok) break;
-                v_ready = true;
-              }
-              ok = mbar_wait(smem_u32(&sm.p_full[s]), pcnt[s] & 1, p.limit_ns, abort);
-              if (!ok) break;
-              ++pcnt[s];
-              tc_fence_after();
-              issue_pv(s, j - 1, prev_slot);
-              if (j == it.n[s]) tc_commit(smem_u32(&sm.o_full[s]));
-            }
-            if (j < it.n[s]) {
-              const uint32_t qbase = smem_u32(sm.q[s]);
-              const uint32_t kbase = smem_u32(sm.k[slot]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          // K-major, 128B swizzle: advance 32 bytes per 16-element K step
+          // inside the swizzle row; 8-row groups 1024 B apart.
+          const uint64_t adesc = sdesc_sw128(qbase + kk * 32, 16, 1024);
+          const uint64_t bdesc = sdesc_sw128(kbase + kk * 32, 16, 1024);
+          mma_ss(tmem + col_s(s), adesc, bdesc, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&sm.s_full[s]));
+        if (last) tc_commit(smem_u32(&sm.q_empty[s]));
+        ++sc;
+      };
+      // PV_s(j) with V in ring slot g; j = 0 overwrites O_s.
+      auto issue_pv = [&](int s, uint32_t g, int j) {
+        uint32_t& pc = s == 0 ? pc0 : pc1;
+        if (!wait(sm.p_full[s], pc & 1)) return;
+        tc_fence_after();
+        const uint32_t vbase = smem_u32(sm.v[g % STAGES]);
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                // K-major, 128B swizzle: advance 32 bytes per 16-element K step
-                // inside the swizzle row; 8-row groups 1024 B apart.
-                const uint64_t adesc = sdesc_sw128(qbase + kk * 32, 16, 1024);
-                const uint64_t bdesc = sdesc_sw128(kbase + kk * 32, 16, 1024);
-                mma_ss(tmem + col_s(s), adesc, bdesc, IDESC_S, kk > 0 ? 1u : 0u);
-              }
-              tc_commit(smem_u32(&sm.s_full[s]));
-            }
-          }
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          // B = V rows kk*16 .. kk*16+15 (K dim = keys), MN-major, 128B swizzle:
+          // 8-row groups 1024 B apart (SBO).  N = 64 is a single 128-byte swizzle
+          // atom, so the MN-direction stride (LBO) is never applied; it is set to
+          // the same 1024 B so that no reading of the fields leaves the tile.
+          const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, 1024, 1024);
+          mma_ts(tmem + col_o(s), tmem + col_p(s) + kk * 8, bdesc, IDESC_O,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&sm.pv_done[s]));
+        ++pc;
+      };
+      // First round of an item: Q tiles in, S_s(0) for both stages.
+      auto start_item = [&](const Item& it, uint32_t g0, uint32_t items) {
+        for (int s = 0; s < QT; ++s) wait(sm.q_full[s], items & 1);
+        if (!ok) return;
+        const int nmax = max(it.n[0], it.n[1]);
+        if (nmax > 0 && !wait(sm.k_full[g0 % STAGES], (g0 / STAGES) & 1)) return;
+        for (int s = 0; s < QT && ok; ++s) {
+          if (it.n[s] > 0)
+            issue_s(s, g0, it.n[s] == 1);
+          else
+            tc_commit(smem_u32(&sm.q_empty[s]));  // nothing to do for this Q tile
+        }
+        if (ok && nmax > 0) tc_commit(smem_u32(&sm.k_empty[g0 % STAGES]));
+      };
+
+      int t = blockIdx.x;
+      uint32_t g0 = 0, items = 0;
+      Item it;
+      if (t < p.num_items) {
+        it = decode_item(p, t);
+        start_item(it, g0, items);
+      }
+      while (ok && t < p.num_items) {
+        const int nmax = max(it.n[0], it.n[1]);
+        for (int j = 1; j < nmax && ok; ++j) {
+          const uint32_t g = g0 + j;
+          if (!wait(sm.k_full[g % STAGES], (g / STAGES) & 1)) break;
+          for (int s = 0; s < QT && ok; ++s)
+            if (j < it.n[s]) issue_s(s, g, j == it.n[s] - 1);
           if (!ok) break;
-          tc_commit(smem_u32(&sm.k_empty[slot]));
-          if (j > 0) tc_commit(smem_u32(&sm.v_empty[prev_slot]));
-          prev_slot = slot;
-          prev_ph = ph;
+          tc_commit(smem_u32(&sm.k_empty[g % STAGES]));
+          if (!wait(sm.v_full[(g - 1) % STAGES], ((g - 1) / STAGES) & 1)) break;
+          for (int s = 0; s < QT && ok; ++s)
+            if (j - 1 < it.n[s]) issue_pv(s, g - 1, j - 1);
+          if (!ok) break;
+          tc_commit(smem_u32(&sm.v_empty[(g - 1) % STAGES]));
         }
         if (!ok) break;
-        for (int s = 0; s < QT; ++s) tc_commit(smem_u32(&sm.q_empty[s]));
-        if (nmax > 0) {
-          bool v_ready = false;
-          for (int s = 0; s < QT && ok; ++s) {
-            if (it.n[s] != nmax) continue;
-            if (!v_ready) {
-              ok = mbar_wait(smem_u32(&sm.v_full[prev_slot]), prev_ph, p.limit_ns, abort);
-              if (!ok) break;
-              v_ready = true;
-            }
-            ok = mbar_wait(smem_u32(&sm.p_full[s]), pcnt[s] & 1, p.limit_ns, abort);
-            if (!ok) break;
-            ++pcnt[s];
-            tc_fence_after();
-            issue_pv(s, nmax - 1, prev_slot);
-            tc_commit(smem_u32(&sm.o_full[s]));
-          }
+        const int t_next = t + gridDim.x;
+        Item it_next;
+        if (t_next < p.num_items) {
+          it_next = decode_item(p, t_next);
+          start_item(it_next, g0 + nmax, items + 1);
           if (!ok) break;
-          tc_commit(smem_u32(&sm.v_empty[prev_slot]));
         }
+        if (nmax > 0) {
+          const uint32_t g = g0 + nmax - 1;
+          if (!wait(sm.v_full[g % STAGES], (g / STAGES) & 1)) break;
+          for (int s = 0; s < QT && ok; ++s)
+            if (nmax - 1 < it.n[s]) issue_pv(s, g, nmax - 1);
+          if (!ok) break;
+          tc_commit(smem_u32(&sm.v_empty[g % STAGES]));
+        }
+        t = t_next;
+        it = it_next;
+        g0 += nmax;
+        ++items;
       }
       if (!ok) record_timeout(p, sm);
       // every MMA issued by this thread completes before tensor memory is freed
@@ -319,7 +351,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int never = 0;
       mbar_wait(smem_u32(&sm.drain), 0, p.limit_ns, &never);
     }
+  }
   } else {
+    setmaxnreg_inc<SOFTMAX_REGS>();
     // ------------------------------------------------------------ softmax
     const int s = warp >> 2;
     const int quarter = warp & 3;
@@ -329,7 +363,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tP = tmem + lane_off + col_p(s);
     const bool causal = p.mask == kMaskCausal;
     const float c = p.scale_log2;
-    uint32_t scnt = 0, ocnt = 0;
+    uint32_t u = 0;  // tiles this stage has processed (all items)
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
       const Item it = decode_item(p, t);
@@ -337,11 +371,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int row = row0 + quarter * 32 + lane;
       float m = -INFINITY;  // running max of scale*log2(e)*score (possibly stale)
       float l = 0.f;        // running sum of 2^(x - m)
-      for (int j = 0; j < it.n[s]; ++j) {
-        ok = mbar_wait(smem_u32(&sm.s_full[s]), scnt & 1, p.limit_ns, abort);
+      for (int j = 0; j < it.n[s]; ++j, ++u) {
+        ok = mbar_wait(smem_u32(&sm.s_full[s]), u & 1, p.limit_ns, abort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        ++scnt;
         tc_fence_after();
         uint32_t r[4][32];
         tmem_ld32(tS + 0, r[0]);
@@ -352,6 +385,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         reg_fence(r[1]);
         reg_fence(r[2]);
         reg_fence(r[3]);
+        // S is in registers: the next S product may overwrite its columns.
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.s_free[s]));
 
         const int kbase = j * BN;
         if (kbase + BN > it.key_limit || (causal && kbase + BN - 1 > row0)) {
@@ -364,17 +400,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (q4 * 32 + i >= lim) r[q4][i] = __float_as_uint(-INFINITY);
         }
 
-        float mx[8];
+        float mx[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+        for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[q4][i]));
-        const float rowmax =
-            fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        const float mt = rowmax * c;
+          for (int i = 0; i < 32; i += 8) {
+            mx[0] = max3(mx[0], __uint_as_float(r[q4][i + 0]), __uint_as_float(r[q4][i + 1]));
+            mx[1] = max3(mx[1], __uint_as_float(r[q4][i + 2]), __uint_as_float(r[q4][i + 3]));
+            mx[2] = max3(mx[2], __uint_as_float(r[q4][i + 4]), __uint_as_float(r[q4][i + 5]));
+            mx[3] = max3(mx[3], __uint_as_float(r[q4][i + 6]), __uint_as_float(r[q4][i + 7]));
+          }
+        const float mt = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]) * c;
 
         bool rescale_o = false;
         float alpha = 1.f;
@@ -384,39 +422,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           rescale_o = j > 0;
           m = mt;
         }
-        if (__any_sync(0xffffffffu, rescale_o)) {
-          // O_s is stable here: s_full of tile j is committed after PV(j-1).
-          uint32_t o0[32], o1[32];
-          tmem_ld32(tO, o0);
-          tmem_ld32(tO + 32, o1);
-          tmem_ld_wait(o0);
-          reg_fence(o1);
-          const float a = rescale_o ? alpha : 1.f;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            o0[i] = __float_as_uint(__uint_as_float(o0[i]) * a);
-            o1[i] = __float_as_uint(__uint_as_float(o1[i]) * a);
-          }
-          tmem_st32(tO, o0);
-          tmem_st32(tO + 32, o1);
-        }
 
         const float neg_m = (m == -INFINITY) ? 0.f : -m;
-        float ls[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ls[i] = 0.f;
+        float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
         uint32_t pk[2][32];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float p0 = ex2(fmaf(__uint_as_float(r[q4][i]), c, neg_m));
-            const float p1 = ex2(fmaf(__uint_as_float(r[q4][i + 1]), c, neg_m));
-            ls[(i >> 1) & 7] += p0 + p1;
+          for (int i = 0; i < 32; i += 4) {
+            float x0, x1, x2, x3;
+            fma2(x0, x1, __uint_as_float(r[q4][i]), __uint_as_float(r[q4][i + 1]), c, c, neg_m,
+                 neg_m);
+            fma2(x2, x3, __uint_as_float(r[q4][i + 2]), __uint_as_float(r[q4][i + 3]), c, c,
+                 neg_m, neg_m);
+            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+            add2(ls0, ls1, ls0, ls1, p0, p1);
+            add2(ls2, ls3, ls2, ls3, p2, p3);
             pk[q4 >> 1][(q4 & 1) * 16 + (i >> 1)] = pack_bf16x2(p0, p1);
+            pk[q4 >> 1][(q4 & 1) * 16 + (i >> 1) + 1] = pack_bf16x2(p2, p3);
           }
         }
-        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+        l += (ls0 + ls1) + (ls2 + ls3);
+
+        // P(u) overwrites P(u-1) and O may be rescaled only once PV(u-1) is done.
+        if (u > 0) {
+          ok = mbar_wait(smem_u32(&sm.pv_done[s]), (u - 1) & 1, p.limit_ns, abort);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          const float a = rescale_o ? alpha : 1.f;
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t oc[32];
+            tmem_ld32(tO + h2 * 32, oc);
+            tmem_ld_wait(oc);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) oc[i] = __float_as_uint(__uint_as_float(oc[i]) * a);
+            tmem_st32(tO + h2 * 32, oc);
+          }
+        }
         tmem_st32(tP, pk[0]);
         tmem_st32(tP + 32, pk[1]);
         tmem_st_wait();
@@ -428,10 +474,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ---------------------------------------------------------- epilogue
       uint32_t o0[32], o1[32];
       if (it.n[s] > 0) {
-        ok = mbar_wait(smem_u32(&sm.o_full[s]), ocnt & 1, p.limit_ns, abort);
+        ok = mbar_wait(smem_u32(&sm.pv_done[s]), (u - 1) & 1, p.limit_ns, abort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        ++ocnt;
         tc_fence_after();
         tmem_ld32(tO, o0);
         tmem_ld32(tO + 32, o1);
@@ -445,22 +490,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float inv = l > 0.f ? 1.f / l : 0.f;
         uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(it.bh) * p.n_q + row) * D);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < 8; ++g) {
+          const uint32_t* src = g < 4 ? o0 + g * 8 : o1 + (g - 4) * 8;
           uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(o0[g * 8 + 0]) * inv, __uint_as_float(o0[g * 8 + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(o0[g * 8 + 2]) * inv, __uint_as_float(o0[g * 8 + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(o0[g * 8 + 4]) * inv, __uint_as_float(o0[g * 8 + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(o0[g * 8 + 6]) * inv, __uint_as_float(o0[g * 8 + 7]) * inv);
+          w.x = pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
           dst[g] = w;
-        }
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(o1[g * 8 + 0]) * inv, __uint_as_float(o1[g * 8 + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(o1[g * 8 + 2]) * inv, __uint_as_float(o1[g * 8 + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(o1[g * 8 + 4]) * inv, __uint_as_float(o1[g * 8 + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(o1[g * 8 + 6]) * inv, __uint_as_float(o1[g * 8 + 7]) * inv);
-          dst[4 + g] = w;
         }
         if (p.lse != nullptr)
           p.lse[static_cast<size_t>(it.bh) * p.n_q + row] =
@@ -500,7 +537,13 @@ cudaError_t launch_fwd_tc(const Problem& pb, const CUtensorMap& tmq, const CUten
   p.limit_ns = ctx.limit_ns;
   p.status = ctx.status;
   const size_t smem = fwd_tc_smem_bytes();
-  cudaError_t err = cudaFuncSetAttribute(attn_fwd_tc_kernel,
+  // The register hand-over inside the kernel assumes the launch holds
+  // LAUNCH_REGS per thread; refuse to launch a build that does not.
+  cudaFuncAttributes attr;
+  cudaError_t err = cudaFuncGetAttributes(&attr, attn_fwd_tc_kernel);
+  if (err != cudaSuccess) return err;
+  if (attr.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+  err = cudaFuncSetAttribute(attn_fwd_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
