@@ -9,7 +9,7 @@
 #include <cmath>
 #include <mutex>
 
-#include "../../include/attn.h"
+#include "attn.h"
 #include "attn_internal.cuh"
 
 namespace attn {

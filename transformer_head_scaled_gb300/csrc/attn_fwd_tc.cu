@@ -15,9 +15,10 @@
 //   warps 0-3  softmax of Q tile 0 (rows 0-127 of a 256-row work item),
 //              one thread per row = one tensor-memory lane;
 //   warps 4-7  softmax of Q tile 1 (rows 128-255);
-//   warp  8    TMA producer (Q tiles per item, a 3-deep K and V ring);
-//   warp  9    tensor-memory owner and single-thread MMA issuer;
-//   warps 10-11 idle (they only complete the producer warpgroup).
+//   warp  8    TMA producer of the Q tiles and the K ring (4 deep);
+//   warp  9    tensor-memory owner and MMA issuer of Q tile 0;
+//   warp  10   TMA producer of the V ring (5 deep);
+//   warp  11   MMA issuer of Q tile 1.
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   S0 [0,128)  S1 [128,256)  O0 [256,320)  O1 [320,384)  P0 [384,448)  P1 [448,512)
 // The MMA issue order per KV tile j is  PV0(j-1), S0(j), PV1(j-1), S1(j):
@@ -40,17 +41,20 @@ constexpr int QT = 2;        // Q tiles per work item
 constexpr int ROWS = BM * QT;
 constexpr int BN = 128;      // keys per K/V tile
 constexpr int D = 64;        // head size
-constexpr int STAGES = 3;    // K/V ring depth
+constexpr int KSTAGES = 4;   // K ring depth
+constexpr int VSTAGES = 5;   // V ring depth (a V tile is held about two tiles longer than a K tile)
 constexpr uint32_t TILE_BYTES = BM * D * 2;  // a Q, K or V tile: 16 KB
 constexpr int LOAD_WARP = 8;
 constexpr int MMA_WARP = 9;
+constexpr int VLOAD_WARP = 10;
+constexpr int MMA1_WARP = 11;
 constexpr int NUM_THREADS = 384;  // 3 warpgroups: softmax 0, softmax 1, producer + MMA
 // Launched at 168 registers a thread (65536 / 384, rounded down to a multiple
 // of 8); the producer warpgroup hands registers to the two softmax
-// warpgroups: 2 * 208 + 80 <= 3 * 168.
+// warpgroups: 2 * 184 + 136 <= 3 * 168.
 constexpr int LAUNCH_REGS = 168;
-constexpr uint32_t SOFTMAX_REGS = 208;
-constexpr uint32_t PRODUCER_REGS = 80;
+constexpr uint32_t SOFTMAX_REGS = 184;
+constexpr uint32_t PRODUCER_REGS = 136;
 static_assert(2 * SOFTMAX_REGS + PRODUCER_REGS <= 3 * LAUNCH_REGS, "register split");
 constexpr uint32_t TMEM_COLS = 512;
 // Keep a stale running max until the row max has grown by more than 2^8:
@@ -65,13 +69,13 @@ __host__ __device__ constexpr uint32_t col_p(int s) { return 384u + 64u * s; }
 
 struct __align__(1024) Smem {
   uint8_t q[QT][TILE_BYTES];
-  uint8_t k[STAGES][TILE_BYTES];
-  uint8_t v[STAGES][TILE_BYTES];
+  uint8_t k[KSTAGES][TILE_BYTES];
+  uint8_t v[VSTAGES][TILE_BYTES];
   uint64_t q_full[QT], q_empty[QT];
-  uint64_t k_full[STAGES], k_empty[STAGES];
-  uint64_t v_full[STAGES], v_empty[STAGES];
+  uint64_t k_full[KSTAGES], k_empty[KSTAGES];
+  uint64_t v_full[VSTAGES], v_empty[VSTAGES];
   uint64_t s_full[QT], s_free[QT], p_full[QT], pv_done[QT];
-  uint64_t drain;
+  uint64_t drain[QT];
   uint32_t tmem_base;
   int abort;
 };
@@ -155,13 +159,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(smem_u32(&sm.p_full[s]), BM);
       mbar_init(smem_u32(&sm.pv_done[s]), 1);
     }
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < KSTAGES; ++i) {
       mbar_init(smem_u32(&sm.k_full[i]), 1);
-      mbar_init(smem_u32(&sm.k_empty[i]), 1);
-      mbar_init(smem_u32(&sm.v_full[i]), 1);
-      mbar_init(smem_u32(&sm.v_empty[i]), 1);
+      mbar_init(smem_u32(&sm.k_empty[i]), QT);  // one arrival per Q tile
     }
-    mbar_init(smem_u32(&sm.drain), 1);
+    for (int i = 0; i < VSTAGES; ++i) {
+      mbar_init(smem_u32(&sm.v_full[i]), 1);
+      mbar_init(smem_u32(&sm.v_empty[i]), QT);
+    }
+    for (int s = 0; s < QT; ++s) mbar_init(smem_u32(&sm.drain[s]), 1);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -181,16 +187,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp >= LOAD_WARP) {
     setmaxnreg_dec<PRODUCER_REGS>();
-   if (warp == LOAD_WARP) {
-    // ------------------------------------------------------------ producer
+   if (warp == LOAD_WARP || warp == VLOAD_WARP) {
+    // ------------------------------------------------------------ producers
+    // warp 8: Q tiles of every item and the K ring; warp 10: the V ring.
+    // Separate threads, so that a V tile waiting for a free slot never holds
+    // back the K tiles behind it.
     if (lane == 0) {
-      uint32_t kv = 0;
+      const bool is_v = warp == VLOAD_WARP;
+      const int stages = is_v ? VSTAGES : KSTAGES;
+      uint64_t* full = is_v ? sm.v_full : sm.k_full;
+      uint64_t* empty = is_v ? sm.v_empty : sm.k_empty;
+      uint8_t* ring = is_v ? &sm.v[0][0] : &sm.k[0][0];
+      const CUtensorMap* map = is_v ? &tmv : &tmk;
+      uint32_t cnt = 0;
       uint32_t items = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x, ++items) {
         const Item it = decode_item(p, t);
         const int nmax = max(it.n[0], it.n[1]);
-        for (int s = 0; s < QT && ok; ++s) {
+        for (int s = 0; s < QT && ok && !is_v; ++s) {
           ok = mbar_wait(smem_u32(&sm.q_empty[s]), (items & 1) ^ 1, p.limit_ns, abort);
           if (!ok) break;
           const uint32_t bar = smem_u32(&sm.q_full[s]);
@@ -201,16 +216,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive(bar);
           }
         }
-        for (int j = 0; j < nmax && ok; ++j, ++kv) {
-          const uint32_t slot = kv % STAGES, ph = (kv / STAGES) & 1;
-          ok = mbar_wait(smem_u32(&sm.k_empty[slot]), ph ^ 1, p.limit_ns, abort);
+        for (int j = 0; j < nmax && ok; ++j) {
+          const uint32_t slot = cnt % stages, ph = (cnt / stages) & 1;
+          ok = mbar_wait(smem_u32(&empty[slot]), ph ^ 1, p.limit_ns, abort);
           if (!ok) break;
-          mbar_arrive_expect_tx(smem_u32(&sm.k_full[slot]), TILE_BYTES);
-          tma_load_3d(smem_u32(sm.k[slot]), &tmk, smem_u32(&sm.k_full[slot]), 0, j * BN, it.bh);
-          ok = mbar_wait(smem_u32(&sm.v_empty[slot]), ph ^ 1, p.limit_ns, abort);
-          if (!ok) break;
-          mbar_arrive_expect_tx(smem_u32(&sm.v_full[slot]), TILE_BYTES);
-          tma_load_3d(smem_u32(sm.v[slot]), &tmv, smem_u32(&sm.v_full[slot]), 0, j * BN, it.bh);
+          mbar_arrive_expect_tx(smem_u32(&full[slot]), TILE_BYTES);
+          tma_load_3d(smem_u32(ring + slot * TILE_BYTES), map, smem_u32(&full[slot]), 0, j * BN,
+                      it.bh);
+          ++cnt;
         }
       }
       if (!ok) {
@@ -219,137 +232,113 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // goes away: wait (bounded, ignoring the abort flag) for the last
         // phase armed on every full barrier.
         const int never = 0;
-        for (uint32_t i = 0; i < STAGES; ++i) {
-          const uint32_t uses = kv / STAGES + (i < kv % STAGES ? 1u : 0u);
-          if (uses > 0) {
-            mbar_wait(smem_u32(&sm.k_full[i]), (uses - 1) & 1, p.limit_ns, &never);
-            mbar_wait(smem_u32(&sm.v_full[i]), (uses - 1) & 1, p.limit_ns, &never);
-          }
+        for (int i = 0; i < stages; ++i) {
+          const uint32_t uses = cnt / stages + (static_cast<uint32_t>(i) < cnt % stages ? 1u : 0u);
+          if (uses > 0) mbar_wait(smem_u32(&full[i]), (uses - 1) & 1, p.limit_ns, &never);
         }
-        for (int s = 0; s < QT; ++s)
+        for (int s = 0; s < QT && !is_v; ++s)
           if (items > 0) mbar_wait(smem_u32(&sm.q_full[s]), (items - 1) & 1, p.limit_ns, &never);
       }
     }
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
-    // Fixed issue order, one round per K/V tile j of an item:
-    //   S0(j), S1(j), PV0(j-1), PV1(j-1)
-    // S_s(j) waits only until softmax s has copied S_s(j-1) into registers
-    // (s_free), so the next scores are computed while the softmax of the
-    // previous tile runs; PV_s(j-1) waits for P_s(j-1) (p_full).  The next
-    // item's S(0) products go before this item's last PV products.
+  } else if (warp == MMA_WARP || warp == MMA1_WARP) {
+    // ------------------------------------------------------------ MMA issuers
+    // One issuing thread per Q tile s (warp 9: s = 0, warp 11: s = 1), so
+    // that a thread blocked on a busy tensor pipe never delays the other
+    // tile's products.  Tile s runs through its K/V tiles u = 0, 1, ... (all
+    // items of this CTA) in the order S(0), S(1), PV(0), S(2), PV(1), ...:
+    // S(u) goes as soon as the softmax has copied S(u-1) into registers
+    // (s_free), PV(u-1) right after it, once P(u-1) is in tensor memory
+    // (p_full).  That is the order in which these events happen, so blocking
+    // waits lose nothing.  Every K/V ring slot is released by one arrival per
+    // Q tile: a commit when the tile was used, a plain arrive when not.
     if (lane == 0) {
+      const int s = warp == MMA_WARP ? 0 : 1;
       constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
       constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, false, true);    // V is MN-major
-      uint32_t sc0 = 0, sc1 = 0;  // S products issued per stage (all items)
-      uint32_t pc0 = 0, pc1 = 0;  // PV products issued per stage
-      bool ok = true;
+      constexpr uint32_t TILE16 = TILE_BYTES >> 4;  // a tile step in descriptor units
+      // K-major, 128B swizzle, 8-row groups 1024 B apart; a 16-element K step
+      // is 32 bytes inside the swizzle row (+2 in descriptor units).
+      const uint64_t dq = sdesc_sw128(smem_u32(sm.q[s]), 16, 1024);
+      const uint64_t dk = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
+      // V is the MN-major B operand: 16 keys (one K step) are 16 rows of
+      // 128 B (+128 in descriptor units); 8-row groups 1024 B apart (SBO).
+      // N = 64 is a single 128-byte swizzle atom, so the MN-direction stride
+      // (LBO) is never applied; it is set to the same 1024 B so that no
+      // reading of the fields leaves the tile.
+      const uint64_t dv = sdesc_sw128(smem_u32(sm.v[0]), 1024, 1024);
+      const uint32_t t_s = tmem + col_s(s), t_o = tmem + col_o(s), t_p = tmem + col_p(s);
 
-      auto wait = [&](uint64_t& bar, uint32_t parity) {
-        if (ok) ok = mbar_wait(smem_u32(&bar), parity, p.limit_ns, abort);
+      bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (ok) ok = mbar_wait(smem_u32(bar), parity, p.limit_ns, abort);
         return ok;
       };
-      // S_s(j) for the tile in ring slot g; `last` releases Q tile s.
-      auto issue_s = [&](int s, uint32_t g, bool last) {
-        uint32_t& sc = s == 0 ? sc0 : sc1;
-        if (sc > 0 && !wait(sm.s_free[s], (sc - 1) & 1)) return;
+      auto k_wait = [&](uint32_t g) { return wait(&sm.k_full[g % KSTAGES], (g / KSTAGES) & 1); };
+      auto v_wait = [&](uint32_t g) { return wait(&sm.v_full[g % VSTAGES], (g / VSTAGES) & 1); };
+      uint32_t u = 0;        // S products issued by this Q tile (all items)
+      uint32_t npv = 0;      // PV products issued
+      bool pending = false;  // the last S'd tile still owes its PV product
+      uint32_t pg = 0;       // its ring index
+      int pj = 0;            // its index inside its item
+      // PV of the pending tile: P from tensor memory times V; an item's first
+      // product overwrites O.
+      auto flush_pv = [&]() {
+        if (!pending || !wait(&sm.p_full[s], npv & 1) || !v_wait(pg)) return;
         tc_fence_after();
-        const uint32_t qbase = smem_u32(sm.q[s]);
-        const uint32_t kbase = smem_u32(sm.k[g % STAGES]);
+        const uint64_t b = dv + (pg % VSTAGES) * TILE16;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          // K-major, 128B swizzle: advance 32 bytes per 16-element K step
-          // inside the swizzle row; 8-row groups 1024 B apart.
-          const uint64_t adesc = sdesc_sw128(qbase + kk * 32, 16, 1024);
-          const uint64_t bdesc = sdesc_sw128(kbase + kk * 32, 16, 1024);
-          mma_ss(tmem + col_s(s), adesc, bdesc, IDESC_S, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(smem_u32(&sm.s_full[s]));
-        if (last) tc_commit(smem_u32(&sm.q_empty[s]));
-        ++sc;
-      };
-      // PV_s(j) with V in ring slot g; j = 0 overwrites O_s.
-      auto issue_pv = [&](int s, uint32_t g, int j) {
-        uint32_t& pc = s == 0 ? pc0 : pc1;
-        if (!wait(sm.p_full[s], pc & 1)) return;
-        tc_fence_after();
-        const uint32_t vbase = smem_u32(sm.v[g % STAGES]);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // B = V rows kk*16 .. kk*16+15 (K dim = keys), MN-major, 128B swizzle:
-          // 8-row groups 1024 B apart (SBO).  N = 64 is a single 128-byte swizzle
-          // atom, so the MN-direction stride (LBO) is never applied; it is set to
-          // the same 1024 B so that no reading of the fields leaves the tile.
-          const uint64_t bdesc = sdesc_sw128(vbase + kk * 16 * 128, 1024, 1024);
-          mma_ts(tmem + col_o(s), tmem + col_p(s) + kk * 8, bdesc, IDESC_O,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(t_o, t_p + kk * 8, b + 128 * kk, IDESC_O, (pj > 0 || kk > 0) ? 1u : 0u);
         tc_commit(smem_u32(&sm.pv_done[s]));
-        ++pc;
-      };
-      // First round of an item: Q tiles in, S_s(0) for both stages.
-      auto start_item = [&](const Item& it, uint32_t g0, uint32_t items) {
-        for (int s = 0; s < QT; ++s) wait(sm.q_full[s], items & 1);
-        if (!ok) return;
-        const int nmax = max(it.n[0], it.n[1]);
-        if (nmax > 0 && !wait(sm.k_full[g0 % STAGES], (g0 / STAGES) & 1)) return;
-        for (int s = 0; s < QT && ok; ++s) {
-          if (it.n[s] > 0)
-            issue_s(s, g0, it.n[s] == 1);
-          else
-            tc_commit(smem_u32(&sm.q_empty[s]));  // nothing to do for this Q tile
-        }
-        if (ok && nmax > 0) tc_commit(smem_u32(&sm.k_empty[g0 % STAGES]));
+        tc_commit(smem_u32(&sm.v_empty[pg % VSTAGES]));
+        ++npv;
+        pending = false;
       };
 
-      int t = blockIdx.x;
       uint32_t g0 = 0, items = 0;
-      Item it;
-      if (t < p.num_items) {
-        it = decode_item(p, t);
-        start_item(it, g0, items);
-      }
-      while (ok && t < p.num_items) {
+      for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x, ++items) {
+        const Item it = decode_item(p, t);
+        const int n = it.n[s];
         const int nmax = max(it.n[0], it.n[1]);
-        for (int j = 1; j < nmax && ok; ++j) {
+        if (!wait(&sm.q_full[s], items & 1)) break;
+        if (n == 0) tc_commit(smem_u32(&sm.q_empty[s]));
+        for (int j = 0; j < n && ok; ++j) {
           const uint32_t g = g0 + j;
-          if (!wait(sm.k_full[g % STAGES], (g / STAGES) & 1)) break;
-          for (int s = 0; s < QT && ok; ++s)
-            if (j < it.n[s]) issue_s(s, g, j == it.n[s] - 1);
-          if (!ok) break;
-          tc_commit(smem_u32(&sm.k_empty[g % STAGES]));
-          if (!wait(sm.v_full[(g - 1) % STAGES], ((g - 1) / STAGES) & 1)) break;
-          for (int s = 0; s < QT && ok; ++s)
-            if (j - 1 < it.n[s]) issue_pv(s, g - 1, j - 1);
-          if (!ok) break;
-          tc_commit(smem_u32(&sm.v_empty[(g - 1) % STAGES]));
+          if (!k_wait(g)) break;
+          if (u > 0 && !wait(&sm.s_free[s], (u - 1) & 1)) break;
+          tc_fence_after();
+          const uint64_t b = dk + (g % KSTAGES) * TILE16;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(t_s, dq + 2 * kk, b + 2 * kk, IDESC_S, kk > 0 ? 1u : 0u);
+          tc_commit(smem_u32(&sm.s_full[s]));
+          tc_commit(smem_u32(&sm.k_empty[g % KSTAGES]));
+          if (j == n - 1) tc_commit(smem_u32(&sm.q_empty[s]));  // Q tile s no longer read
+          ++u;
+          flush_pv();  // the previous tile's PV goes right after this S product
+          pending = true;
+          pg = g;
+          pj = j;
         }
         if (!ok) break;
-        const int t_next = t + gridDim.x;
-        Item it_next;
-        if (t_next < p.num_items) {
-          it_next = decode_item(p, t_next);
-          start_item(it_next, g0 + nmax, items + 1);
-          if (!ok) break;
+        if (n < nmax) {
+          // Tiles this Q tile skips: settle the pending product first (its V
+          // slot may be the next one the loader needs), then release them.
+          flush_pv();
+          for (int j = n; j < nmax && ok; ++j) {
+            const uint32_t g = g0 + j;
+            if (k_wait(g)) mbar_arrive(smem_u32(&sm.k_empty[g % KSTAGES]));
+            if (v_wait(g)) mbar_arrive(smem_u32(&sm.v_empty[g % VSTAGES]));
+          }
         }
-        if (nmax > 0) {
-          const uint32_t g = g0 + nmax - 1;
-          if (!wait(sm.v_full[g % STAGES], (g / STAGES) & 1)) break;
-          for (int s = 0; s < QT && ok; ++s)
-            if (nmax - 1 < it.n[s]) issue_pv(s, g, nmax - 1);
-          if (!ok) break;
-          tc_commit(smem_u32(&sm.v_empty[g % STAGES]));
-        }
-        t = t_next;
-        it = it_next;
         g0 += nmax;
-        ++items;
       }
+      flush_pv();
       if (!ok) record_timeout(p, sm);
       // every MMA issued by this thread completes before tensor memory is freed
-      tc_commit(smem_u32(&sm.drain));
+      tc_commit(smem_u32(&sm.drain[s]));
       const int never = 0;
-      mbar_wait(smem_u32(&sm.drain), 0, p.limit_ns, &never);
+      mbar_wait(smem_u32(&sm.drain[s]), 0, p.limit_ns, &never);
     }
   }
   } else {
