@@ -158,13 +158,14 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di)) != ATTN_OK) return rc;
   const long long bh = static_cast<long long>(B) * h;
-  CUtensorMap tmq, tmk, tmv;
+  CUtensorMap tmq, tmk, tmv, tmo;
   if ((rc = encode_3d(&tmq, q, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
   if ((rc = encode_3d(&tmk, k, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
   if ((rc = encode_3d(&tmv, v, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&tmo, o, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
   Problem pb{q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, mask_kind,
              mask_kind == ATTN_MASK_KEY_PADDING ? key_lens : nullptr};
-  cudaError_t e = launch_fwd_tc(pb, tmq, tmk, tmv, make_ctx(*di, stream));
+  cudaError_t e = launch_fwd_tc(pb, tmq, tmk, tmv, tmo, make_ctx(*di, stream));
   if (e != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(1);
   return ATTN_OK;

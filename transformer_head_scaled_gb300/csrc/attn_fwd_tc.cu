@@ -71,6 +71,7 @@ struct __align__(1024) Smem {
   uint8_t q[QT][TILE_BYTES];
   uint8_t k[KSTAGES][TILE_BYTES];
   uint8_t v[VSTAGES][TILE_BYTES];
+  uint8_t o[QT][TILE_BYTES];  // epilogue staging of O for the TMA store
   uint64_t q_full[QT], q_empty[QT];
   uint64_t k_full[KSTAGES], k_empty[KSTAGES];
   uint64_t v_full[VSTAGES], v_empty[VSTAGES];
@@ -142,7 +143,8 @@ __device__ __forceinline__ void record_timeout(const Params& p, Smem& sm) {
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk,
-                       const __grid_constant__ CUtensorMap tmv, const Params p) {
+                       const __grid_constant__ CUtensorMap tmv,
+                       const __grid_constant__ CUtensorMap tmo, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~static_cast<uintptr_t>(1023));
@@ -175,6 +177,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefetch_tmap(&tmq);
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
+    prefetch_tmap(&tmo);
   }
   if (warp == MMA_WARP) {
     tmem_alloc(smem_u32(&sm.tmem_base), TMEM_COLS);
@@ -189,10 +192,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     setmaxnreg_dec<PRODUCER_REGS>();
    if (warp == LOAD_WARP || warp == VLOAD_WARP) {
     // ------------------------------------------------------------ producers
-    // warp 8: Q tiles of every item and the K ring; warp 10: the V ring.
-    // Separate threads, so that a V tile waiting for a free slot never holds
-    // back the K tiles behind it.
-    if (lane == 0) {
+    // warp 8 lane 0: the K ring; warp 8 lane 1: the Q tiles; warp 10: the
+    // V ring.  Separate threads, so that a load waiting for a free buffer
+    // never holds back the loads of the other streams.
+    if (warp == LOAD_WARP && lane == 1) {
+      // Q tiles, one per Q tile s and item, as soon as the previous item's S
+      // products no longer read the buffer.
+      uint32_t items = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x, ++items) {
+        const Item it = decode_item(p, t);
+        for (int s = 0; s < QT && ok; ++s) {
+          ok = mbar_wait(smem_u32(&sm.q_empty[s]), (items & 1) ^ 1, p.limit_ns, abort);
+          if (!ok) break;
+          const uint32_t bar = smem_u32(&sm.q_full[s]);
+          if (it.n[s] > 0) {
+            mbar_arrive_expect_tx(bar, TILE_BYTES);
+            tma_load_3d(smem_u32(sm.q[s]), &tmq, bar, 0, it.qb * ROWS + s * BM, it.bh);
+          } else {
+            mbar_arrive(bar);
+          }
+        }
+      }
+      if (!ok) {
+        record_timeout(p, sm);
+        const int never = 0;
+        for (int s = 0; s < QT; ++s)
+          if (items > 0) mbar_wait(smem_u32(&sm.q_full[s]), (items - 1) & 1, p.limit_ns, &never);
+      }
+    } else if (lane == 0) {
       const bool is_v = warp == VLOAD_WARP;
       const int stages = is_v ? VSTAGES : KSTAGES;
       uint64_t* full = is_v ? sm.v_full : sm.k_full;
@@ -205,17 +233,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x, ++items) {
         const Item it = decode_item(p, t);
         const int nmax = max(it.n[0], it.n[1]);
-        for (int s = 0; s < QT && ok && !is_v; ++s) {
-          ok = mbar_wait(smem_u32(&sm.q_empty[s]), (items & 1) ^ 1, p.limit_ns, abort);
-          if (!ok) break;
-          const uint32_t bar = smem_u32(&sm.q_full[s]);
-          if (it.n[s] > 0) {
-            mbar_arrive_expect_tx(bar, TILE_BYTES);
-            tma_load_3d(smem_u32(sm.q[s]), &tmq, bar, 0, it.qb * ROWS + s * BM, it.bh);
-          } else {
-            mbar_arrive(bar);
-          }
-        }
         for (int j = 0; j < nmax && ok; ++j) {
           const uint32_t slot = cnt % stages, ph = (cnt / stages) & 1;
           ok = mbar_wait(smem_u32(&empty[slot]), ph ^ 1, p.limit_ns, abort);
@@ -236,8 +253,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t uses = cnt / stages + (static_cast<uint32_t>(i) < cnt % stages ? 1u : 0u);
           if (uses > 0) mbar_wait(smem_u32(&full[i]), (uses - 1) & 1, p.limit_ns, &never);
         }
-        for (int s = 0; s < QT && !is_v; ++s)
-          if (items > 0) mbar_wait(smem_u32(&sm.q_full[s]), (items - 1) & 1, p.limit_ns, &never);
       }
     }
   } else if (warp == MMA_WARP || warp == MMA1_WARP) {
@@ -300,10 +315,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const Item it = decode_item(p, t);
         const int n = it.n[s];
         const int nmax = max(it.n[0], it.n[1]);
+        // The previous item's last PV product goes first unless this item's
+        // first S product is ready to go ahead of it.
+        if (pending && !mbar_test(smem_u32(&sm.q_full[s]), items & 1)) flush_pv();
         if (!wait(&sm.q_full[s], items & 1)) break;
         if (n == 0) tc_commit(smem_u32(&sm.q_empty[s]));
         for (int j = 0; j < n && ok; ++j) {
           const uint32_t g = g0 + j;
+          if (j == 0 && pending &&
+              !mbar_test(smem_u32(&sm.k_full[g % KSTAGES]), (g / KSTAGES) & 1))
+            flush_pv();
           if (!k_wait(g)) break;
           if (u > 0 && !wait(&sm.s_free[s], (u - 1) & 1)) break;
           tc_fence_after();
@@ -475,24 +496,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0u;
       }
-      if (row < p.n_q) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<size_t>(it.bh) * p.n_q + row) * D);
+      // O / l -> bf16 -> this tile's staging buffer in the 128-byte swizzled
+      // layout of the O tensor map -> one TMA store per 128-row tile (rows
+      // past n_q are clipped by the copy).
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int r_local = quarter * 32 + lane;
+      const bool leader = quarter == 0 && lane == 0;
+      if (leader) bulk_wait_read_all();  // the previous store has read the buffer
+      named_bar_sync(1 + s, BM);
+      const uint32_t rbase = smem_u32(sm.o[s]) + r_local * 128;
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const uint32_t* src = g < 4 ? o0 + g * 8 : o1 + (g - 4) * 8;
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
-          dst[g] = w;
-        }
-        if (p.lse != nullptr)
-          p.lse[static_cast<size_t>(it.bh) * p.n_q + row] =
-              l > 0.f ? (m + __log2f(l)) * LN2 : -INFINITY;
+      for (int g = 0; g < 8; ++g) {
+        const uint32_t* src = g < 4 ? o0 + g * 8 : o1 + (g - 4) * 8;
+        st_shared_v4(rbase + ((g ^ (r_local & 7)) << 4),
+                     pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv),
+                     pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv),
+                     pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv),
+                     pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv));
       }
+      fence_proxy_async_smem();
+      named_bar_sync(1 + s, BM);
+      if (leader && row0 < p.n_q) {
+        tma_store_3d(&tmo, smem_u32(sm.o[s]), 0, row0, it.bh);
+        bulk_commit_group();
+      }
+      if (row < p.n_q && p.lse != nullptr)
+        p.lse[static_cast<size_t>(it.bh) * p.n_q + row] =
+            l > 0.f ? (m + __log2f(l)) * LN2 : -INFINITY;
     }
+    // the last stores complete before the CTA (and its shared memory) goes away
+    if (quarter == 0 && lane == 0) bulk_wait_all();
     if (!ok) record_timeout(p, sm);
   }
 
@@ -510,7 +543,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 size_t fwd_tc_smem_bytes() { return sizeof(Smem) + 1024; }
 
 cudaError_t launch_fwd_tc(const Problem& pb, const CUtensorMap& tmq, const CUtensorMap& tmk,
-                          const CUtensorMap& tmv, const LaunchCtx& ctx) {
+                          const CUtensorMap& tmv, const CUtensorMap& tmo, const LaunchCtx& ctx) {
   Params p;
   p.o = static_cast<__nv_bfloat16*>(pb.o);
   p.lse = pb.lse;
@@ -537,7 +570,7 @@ cudaError_t launch_fwd_tc(const Problem& pb, const CUtensorMap& tmq, const CUten
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int grid = p.num_items < ctx.num_sms ? p.num_items : ctx.num_sms;
-  attn_fwd_tc_kernel<<<grid, NUM_THREADS, smem, ctx.stream>>>(tmq, tmk, tmv, p);
+  attn_fwd_tc_kernel<<<grid, NUM_THREADS, smem, ctx.stream>>>(tmq, tmk, tmv, tmo, p);
   return cudaGetLastError();
 }
 

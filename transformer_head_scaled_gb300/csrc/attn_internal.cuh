@@ -34,10 +34,10 @@ struct LaunchCtx {
   cudaStream_t stream;
 };
 
-// tcgen05 bf16 path (d = 64).  The tensor maps describe Q, K, V as 3-D
-// (d, n, B*H) bf16 tensors with a (64, 128, 1) box and 128-byte swizzle.
+// tcgen05 bf16 path (d = 64).  The tensor maps describe Q, K, V and O as
+// 3-D (d, n, B*H) bf16 tensors with a (64, 128, 1) box and 128-byte swizzle.
 cudaError_t launch_fwd_tc(const Problem& pb, const CUtensorMap& tmq, const CUtensorMap& tmk,
-                          const CUtensorMap& tmv, const LaunchCtx& ctx);
+                          const CUtensorMap& tmv, const CUtensorMap& tmo, const LaunchCtx& ctx);
 size_t fwd_tc_smem_bytes();
 
 // fp32 SIMT path (d in {16, 32, 64, 128}).
