@@ -15,9 +15,9 @@
 //   warps 0-3  softmax of Q tile 0 (rows 0-127 of a 256-row work item),
 //              one thread per row = one tensor-memory lane;
 //   warps 4-7  softmax of Q tile 1 (rows 128-255);
-//   warp  8    TMA producer of the Q tiles and the K ring (4 deep);
+//   warp  8    TMA producer of the Q tiles (double-buffered) and the K ring (3 deep);
 //   warp  9    tensor-memory owner and MMA issuer of Q tile 0;
-//   warp  10   TMA producer of the V ring (5 deep);
+//   warp  10   TMA producer of the V ring (4 deep);
 //   warp  11   MMA issuer of Q tile 1.
 // Tensor memory (512 columns x 128 lanes x 32 bit):
 //   S0 [0,128)  S1 [128,256)  O0 [256,320)  O1 [320,384)  P0 [384,448)  P1 [448,512)
@@ -41,8 +41,9 @@ constexpr int QT = 2;        // Q tiles per work item
 constexpr int ROWS = BM * QT;
 constexpr int BN = 128;      // keys per K/V tile
 constexpr int D = 64;        // head size
-constexpr int KSTAGES = 4;   // K ring depth
-constexpr int VSTAGES = 5;   // V ring depth (a V tile is held about two tiles longer than a K tile)
+constexpr int QBUF = 2;      // Q tiles double-buffered: the next item's Q loads during this one
+constexpr int KSTAGES = 3;   // K ring depth
+constexpr int VSTAGES = 4;   // V ring depth (a V tile is held about two tiles longer than a K tile)
 constexpr uint32_t TILE_BYTES = BM * D * 2;  // a Q, K or V tile: 16 KB
 constexpr int LOAD_WARP = 8;
 constexpr int MMA_WARP = 9;
@@ -68,11 +69,11 @@ __host__ __device__ constexpr uint32_t col_o(int s) { return 256u + 64u * s; }
 __host__ __device__ constexpr uint32_t col_p(int s) { return 384u + 64u * s; }
 
 struct __align__(1024) Smem {
-  uint8_t q[QT][TILE_BYTES];
+  uint8_t q[QBUF][QT][TILE_BYTES];
   uint8_t k[KSTAGES][TILE_BYTES];
   uint8_t v[VSTAGES][TILE_BYTES];
   uint8_t o[QT][TILE_BYTES];  // epilogue staging of O for the TMA store
-  uint64_t q_full[QT], q_empty[QT];
+  uint64_t q_full[QBUF][QT], q_empty[QBUF][QT];
   uint64_t k_full[KSTAGES], k_empty[KSTAGES];
   uint64_t v_full[VSTAGES], v_empty[VSTAGES];
   uint64_t s_full[QT], s_free[QT], p_full[QT], pv_done[QT];
@@ -154,8 +155,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < QT; ++s) {
-      mbar_init(smem_u32(&sm.q_full[s]), 1);
-      mbar_init(smem_u32(&sm.q_empty[s]), 1);
+      for (int b = 0; b < QBUF; ++b) {
+        mbar_init(smem_u32(&sm.q_full[b][s]), 1);
+        mbar_init(smem_u32(&sm.q_empty[b][s]), 1);
+      }
       mbar_init(smem_u32(&sm.s_full[s]), 1);
       mbar_init(smem_u32(&sm.s_free[s]), BM);
       mbar_init(smem_u32(&sm.p_full[s]), BM);
@@ -192,35 +195,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     setmaxnreg_dec<PRODUCER_REGS>();
    if (warp == LOAD_WARP || warp == VLOAD_WARP) {
     // ------------------------------------------------------------ producers
-    // warp 8 lane 0: the K ring; warp 8 lane 1: the Q tiles; warp 10: the
-    // V ring.  Separate threads, so that a load waiting for a free buffer
-    // never holds back the loads of the other streams.
-    if (warp == LOAD_WARP && lane == 1) {
-      // Q tiles, one per Q tile s and item, as soon as the previous item's S
-      // products no longer read the buffer.
-      uint32_t items = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x, ++items) {
-        const Item it = decode_item(p, t);
-        for (int s = 0; s < QT && ok; ++s) {
-          ok = mbar_wait(smem_u32(&sm.q_empty[s]), (items & 1) ^ 1, p.limit_ns, abort);
-          if (!ok) break;
-          const uint32_t bar = smem_u32(&sm.q_full[s]);
-          if (it.n[s] > 0) {
-            mbar_arrive_expect_tx(bar, TILE_BYTES);
-            tma_load_3d(smem_u32(sm.q[s]), &tmq, bar, 0, it.qb * ROWS + s * BM, it.bh);
-          } else {
-            mbar_arrive(bar);
-          }
-        }
-      }
-      if (!ok) {
-        record_timeout(p, sm);
-        const int never = 0;
-        for (int s = 0; s < QT; ++s)
-          if (items > 0) mbar_wait(smem_u32(&sm.q_full[s]), (items - 1) & 1, p.limit_ns, &never);
-      }
-    } else if (lane == 0) {
+    // warp 8: the Q tiles (double-buffered) and the K ring; warp 10: the V
+    // ring.  Separate threads, so that a V tile waiting for a free slot never
+    // holds back the K tiles (or the next Q tiles) behind it.
+    if (lane == 0) {
       const bool is_v = warp == VLOAD_WARP;
       const int stages = is_v ? VSTAGES : KSTAGES;
       uint64_t* full = is_v ? sm.v_full : sm.k_full;
@@ -233,6 +211,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x, ++items) {
         const Item it = decode_item(p, t);
         const int nmax = max(it.n[0], it.n[1]);
+        // Q tiles of this item into buffer items % 2 (free once the S
+        // products of item - 2 are done), then its K tiles.
+        const uint32_t qb = items % QBUF, qph = (items / QBUF) & 1;
+        for (int s = 0; s < QT && ok && !is_v; ++s) {
+          ok = mbar_wait(smem_u32(&sm.q_empty[qb][s]), qph ^ 1, p.limit_ns, abort);
+          if (!ok) break;
+          const uint32_t bar = smem_u32(&sm.q_full[qb][s]);
+          if (it.n[s] > 0) {
+            mbar_arrive_expect_tx(bar, TILE_BYTES);
+            tma_load_3d(smem_u32(sm.q[qb][s]), &tmq, bar, 0, it.qb * ROWS + s * BM, it.bh);
+          } else {
+            mbar_arrive(bar);
+          }
+        }
         for (int j = 0; j < nmax && ok; ++j) {
           const uint32_t slot = cnt % stages, ph = (cnt / stages) & 1;
           ok = mbar_wait(smem_u32(&empty[slot]), ph ^ 1, p.limit_ns, abort);
@@ -253,6 +245,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t uses = cnt / stages + (static_cast<uint32_t>(i) < cnt % stages ? 1u : 0u);
           if (uses > 0) mbar_wait(smem_u32(&full[i]), (uses - 1) & 1, p.limit_ns, &never);
         }
+        for (uint32_t b = 0; b < QBUF && !is_v; ++b) {
+          const uint32_t uses = items / QBUF + (b < items % QBUF ? 1u : 0u);
+          for (int s = 0; s < QT && uses > 0; ++s)
+            mbar_wait(smem_u32(&sm.q_full[b][s]), (uses - 1) & 1, p.limit_ns, &never);
+        }
       }
     }
   } else if (warp == MMA_WARP || warp == MMA1_WARP) {
@@ -266,14 +263,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // (p_full).  That is the order in which these events happen, so blocking
     // waits lose nothing.  Every K/V ring slot is released by one arrival per
     // Q tile: a commit when the tile was used, a plain arrive when not.
-    if (lane == 0) {
+    // The whole warp runs the control flow (so that the descriptors live in
+    // uniform registers); one elected lane issues the tcgen05 operations.
+    {
       const int s = warp == MMA_WARP ? 0 : 1;
       constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
       constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, false, true);    // V is MN-major
       constexpr uint32_t TILE16 = TILE_BYTES >> 4;  // a tile step in descriptor units
       // K-major, 128B swizzle, 8-row groups 1024 B apart; a 16-element K step
       // is 32 bytes inside the swizzle row (+2 in descriptor units).
-      const uint64_t dq = sdesc_sw128(smem_u32(sm.q[s]), 16, 1024);
+      const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0][s]), 16, 1024);
+      const uint64_t dq1 = sdesc_sw128(smem_u32(sm.q[1][s]), 16, 1024);
       const uint64_t dk = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
       // V is the MN-major B operand: 16 keys (one K step) are 16 rows of
       // 128 B (+128 in descriptor units); 8-row groups 1024 B apart (SBO).
@@ -283,10 +283,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t dv = sdesc_sw128(smem_u32(sm.v[0]), 1024, 1024);
       const uint32_t t_s = tmem + col_s(s), t_o = tmem + col_o(s), t_p = tmem + col_p(s);
 
+      const bool leader = elect_one();
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t parity) {
-        if (ok) ok = mbar_wait(smem_u32(bar), parity, p.limit_ns, abort);
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, p.limit_ns, abort));
         return ok;
+      };
+      // a barrier test whose answer every lane agrees on
+      auto test = [&](uint64_t* bar, uint32_t parity) {
+        return __shfl_sync(0xffffffffu, mbar_test(smem_u32(bar), parity) ? 1 : 0, 0) != 0;
       };
       auto k_wait = [&](uint32_t g) { return wait(&sm.k_full[g % KSTAGES], (g / KSTAGES) & 1); };
       auto v_wait = [&](uint32_t g) { return wait(&sm.v_full[g % VSTAGES], (g / VSTAGES) & 1); };
@@ -301,11 +306,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!pending || !wait(&sm.p_full[s], npv & 1) || !v_wait(pg)) return;
         tc_fence_after();
         const uint64_t b = dv + (pg % VSTAGES) * TILE16;
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(t_o, t_p + kk * 8, b + 128 * kk, IDESC_O, (pj > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(smem_u32(&sm.pv_done[s]));
-        tc_commit(smem_u32(&sm.v_empty[pg % VSTAGES]));
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(t_o, t_p + kk * 8, b + 128 * kk, IDESC_O, (pj > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(smem_u32(&sm.pv_done[s]));
+          tc_commit(smem_u32(&sm.v_empty[pg % VSTAGES]));
+        }
+        __syncwarp();
         ++npv;
         pending = false;
       };
@@ -317,24 +325,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int nmax = max(it.n[0], it.n[1]);
         // The previous item's last PV product goes first unless this item's
         // first S product is ready to go ahead of it.
-        if (pending && !mbar_test(smem_u32(&sm.q_full[s]), items & 1)) flush_pv();
-        if (!wait(&sm.q_full[s], items & 1)) break;
-        if (n == 0) tc_commit(smem_u32(&sm.q_empty[s]));
+        const uint32_t qb = items % QBUF, qph = (items / QBUF) & 1;
+        const uint64_t dq = qb == 0 ? dq0 : dq1;
+        if (pending && !test(&sm.q_full[qb][s], qph)) flush_pv();
+        if (!wait(&sm.q_full[qb][s], qph)) break;
+        if (n == 0 && leader) tc_commit(smem_u32(&sm.q_empty[qb][s]));
         for (int j = 0; j < n && ok; ++j) {
           const uint32_t g = g0 + j;
-          if (j == 0 && pending &&
-              !mbar_test(smem_u32(&sm.k_full[g % KSTAGES]), (g / KSTAGES) & 1))
-            flush_pv();
+          if (j == 0 && pending && !test(&sm.k_full[g % KSTAGES], (g / KSTAGES) & 1)) flush_pv();
           if (!k_wait(g)) break;
           if (u > 0 && !wait(&sm.s_free[s], (u - 1) & 1)) break;
           tc_fence_after();
           const uint64_t b = dk + (g % KSTAGES) * TILE16;
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(t_s, dq + 2 * kk, b + 2 * kk, IDESC_S, kk > 0 ? 1u : 0u);
-          tc_commit(smem_u32(&sm.s_full[s]));
-          tc_commit(smem_u32(&sm.k_empty[g % KSTAGES]));
-          if (j == n - 1) tc_commit(smem_u32(&sm.q_empty[s]));  // Q tile s no longer read
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(t_s, dq + 2 * kk, b + 2 * kk, IDESC_S, kk > 0 ? 1u : 0u);
+            tc_commit(smem_u32(&sm.s_full[s]));
+            tc_commit(smem_u32(&sm.k_empty[g % KSTAGES]));
+            if (j == n - 1) tc_commit(smem_u32(&sm.q_empty[qb][s]));  // Q tile s no longer read
+          }
+          __syncwarp();
           ++u;
           flush_pv();  // the previous tile's PV goes right after this S product
           pending = true;
@@ -348,16 +359,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           flush_pv();
           for (int j = n; j < nmax && ok; ++j) {
             const uint32_t g = g0 + j;
-            if (k_wait(g)) mbar_arrive(smem_u32(&sm.k_empty[g % KSTAGES]));
-            if (v_wait(g)) mbar_arrive(smem_u32(&sm.v_empty[g % VSTAGES]));
+            if (k_wait(g) && leader) mbar_arrive(smem_u32(&sm.k_empty[g % KSTAGES]));
+            if (v_wait(g) && leader) mbar_arrive(smem_u32(&sm.v_empty[g % VSTAGES]));
           }
         }
         g0 += nmax;
       }
       flush_pv();
-      if (!ok) record_timeout(p, sm);
-      // every MMA issued by this thread completes before tensor memory is freed
-      tc_commit(smem_u32(&sm.drain[s]));
+      if (!ok && leader) record_timeout(p, sm);
+      // every MMA issued by this warp completes before tensor memory is freed
+      if (leader) tc_commit(smem_u32(&sm.drain[s]));
+      __syncwarp();
       const int never = 0;
       mbar_wait(smem_u32(&sm.drain[s]), 0, p.limit_ns, &never);
     }
