@@ -78,6 +78,7 @@ struct __align__(1024) Smem {
   uint64_t v_full[VSTAGES], v_empty[VSTAGES];
   uint64_t s_full[QT], s_free[QT], p_full[QT], pv_done[QT];
   uint64_t drain[QT];
+  uint64_t turn[QT];  // softmax ping-pong: Q tile s may run its exp phase
   uint32_t tmem_base;
   int abort;
 };
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(smem_u32(&sm.v_empty[i]), QT);
     }
     for (int s = 0; s < QT; ++s) mbar_init(smem_u32(&sm.drain[s]), 1);
+    for (int s = 0; s < QT; ++s) mbar_init(smem_u32(&sm.turn[s]), BM);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -386,6 +388,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const bool causal = p.mask == kMaskCausal;
     const float c = p.scale_log2;
     uint32_t u = 0;  // tiles this stage has processed (all items)
+    // Ping-pong: on the tiles both Q tiles visit, the two softmax warpgroups
+    // take turns for the exp phase (the MUFU-bound part), so that one
+    // group's exps overlap the other's max reduction and tensor-memory
+    // traffic instead of competing for the same special-function units.
+    uint32_t turns = 0;
+    if (s == 1) mbar_arrive(smem_u32(&sm.turn[0]));  // Q tile 0 goes first
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
       const Item it = decode_item(p, t);
@@ -445,6 +453,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           m = mt;
         }
 
+        const bool pingpong = j < min(it.n[0], it.n[1]);
+        if (pingpong) {
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(smem_u32(&sm.turn[s]), turns & 1, p.limit_ns, abort));
+          if (!ok) break;
+        }
         const float neg_m = (m == -INFINITY) ? 0.f : -m;
         float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
         uint32_t pk[2][32];
@@ -465,6 +479,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         l += (ls0 + ls1) + (ls2 + ls3);
+        if (pingpong) {
+          mbar_arrive(smem_u32(&sm.turn[s ^ 1]));  // the other Q tile's turn
+          ++turns;
+        }
 
         // P(u) overwrites P(u-1) and O may be rescaled only once PV(u-1) is done.
         if (u > 0) {
