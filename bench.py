@@ -258,12 +258,19 @@ def run_ours(args, w):
     f32 = w.dtype == "f32"
     ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
     klp = None if kl is None else kl.data_ptr()
+    decode = w.kind == "decode"
+    ws_bytes = binding.decode_workspace_bytes(w.B, w.h, w.n_q, w.n_k, w.d) if decode else 0
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
     def step():
-        rc = binding.attn_fwd_raw(*ptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale, w.mask, klp,
-                                  sptr, f32=f32)
+        if decode:
+            rc = binding.attn_decode_raw(*ptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale, klp,
+                                         ws.data_ptr(), ws_bytes, sptr)
+        else:
+            rc = binding.attn_fwd_raw(*ptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale, w.mask, klp,
+                                      sptr, f32=f32)
         if rc != 0:
-            raise binding.AttnError(rc, "attn_fwd")
+            raise binding.AttnError(rc, "attn_decode" if decode else "attn_fwd")
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -300,6 +307,7 @@ def run_ours(args, w):
     value = world * fl / (ms * 1e-3) / 1e12
     peaks = measured_peaks()
     achieved = fl_alg / (ms * 1e-3) / 1e12
+    hbm = inputs.hbm_bytes(w, kl)
 
     # end to end through the public API: pinned host inputs -> device -> attn_fwd -> host
     e2e = run_e2e(args, w, q, k, v, kl, dev, stream, f32)
@@ -314,15 +322,21 @@ def run_ours(args, w):
                    "parallelism": f"dp{world}: batch entries split across ranks, no collective on the data path",
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
                    "flops_per_step": fl, "algorithmic_flops_per_step": fl_alg,
-                   "hbm_bytes_per_step": inputs.hbm_bytes(w), "timed_loop_wall_s": wall},
+                   "hbm_bytes_per_step": hbm, "timed_loop_wall_s": wall},
         "pct_of_peak": 100.0 * (value / world) / peaks["bf16_tflops"],
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                     "traffic": dram_traffic(w.name),
-                     "peak_source": f"{peaks['_source']} bf16_tflops (burst; kernel timed alone)",
-                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                     "hbm_gbs": inputs.hbm_bytes(w) / (ms * 1e-3) / 1e9,
-                     "kernel": "attn_fwd_tc_kernel" if not f32 else "attn_fwd_f32_kernel"},
+        "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                      "traffic": dram_traffic(w.name),
+                      "peak_source": f"{peaks['_source']} bf16_tflops (burst; kernel timed alone)",
+                      "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                      "hbm_gbs": hbm / (ms * 1e-3) / 1e9,
+                      "kernel": "attn_fwd_tc_kernel" if not f32 else "attn_fwd_f32_kernel"}
+                     if not decode else
+                     {"bound": "hbm", "achieved": hbm / (ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                      "unit": "GB/s", "frac": hbm / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                      "traffic": dram_traffic(w.name), "algorithmic_bytes": hbm,
+                      "peak_source": f"{peaks['_source']} hbm_gbs (copy bandwidth)",
+                      "kernel": "attn_decode_split_kernel" + (" + combine" if ws_bytes else "")}),
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": {k2: clk[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons")},
@@ -355,6 +369,9 @@ def run_e2e(args, w, q, k, v, kl, dev, stream, f32):
         0 if hkl is None else hkl.numel() * 4)
     d2h = ho.numel() * ho.element_size() + hl.numel() * 4
     sptr = int(stream.cuda_stream)
+    ws_bytes = (binding.decode_workspace_bytes(w.B, w.h, w.n_q, w.n_k, w.d)
+                if w.kind == "decode" else 0)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
     def step():
         dq.copy_(hq, non_blocking=True)
@@ -362,11 +379,18 @@ def run_e2e(args, w, q, k, v, kl, dev, stream, f32):
         dv.copy_(hv, non_blocking=True)
         if dkl is not None:
             dkl.copy_(hkl, non_blocking=True)
-        rc = binding.attn_fwd_raw(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(),
-                                  dl.data_ptr(), w.B, w.h, w.n_q, w.n_k, w.d, w.scale, w.mask,
-                                  None if dkl is None else dkl.data_ptr(), sptr, f32=f32)
+        if w.kind == "decode":
+            rc = binding.attn_decode_raw(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                         do.data_ptr(), dl.data_ptr(), w.B, w.h, w.n_q, w.n_k,
+                                         w.d, w.scale, None if dkl is None else dkl.data_ptr(),
+                                         ws.data_ptr(), ws_bytes, sptr)
+        else:
+            rc = binding.attn_fwd_raw(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(),
+                                      dl.data_ptr(), w.B, w.h, w.n_q, w.n_k, w.d, w.scale,
+                                      w.mask, None if dkl is None else dkl.data_ptr(), sptr,
+                                      f32=f32)
         if rc != 0:
-            raise binding.AttnError(rc, "attn_fwd")
+            raise binding.AttnError(rc, "attention")
         ho.copy_(do, non_blocking=True)
         hl.copy_(dl, non_blocking=True)
 

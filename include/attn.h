@@ -68,7 +68,9 @@ typedef enum {
  *               otherwise; values are clamped to [0, n_k] on the device.
  *   stream  : cudaStream_t.
  * Scores, softmax and the P.V product are computed in fp32 from bf16 inputs;
- * P is rounded to bf16 before the second product.
+ * P is rounded to bf16 before the second product.  K and V rows past
+ * key_lens[b] never affect the result but must hold finite values: the
+ * tensor-core product multiplies the tail of a partly valid tile by zero.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
              int n_q, int n_k, int d_k, float scale, int mask_kind, const int* key_lens,
@@ -81,6 +83,31 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
                  int h, int n_q, int n_k, int d_k, float scale, int mask_kind,
                  const int* key_lens, struct CUstream_st* stream);
+
+/*
+ * attn_decode -- the same operation for a few new queries against a
+ * key/value cache (an autoregressive decoding step): query i of (b, h) sees
+ * the cached keys j < cache_lens[b].  Bound by HBM bandwidth; runs on the
+ * CUDA cores with TMA-fed tiles and splits each head's cache across CTAs when
+ * B*h alone would leave SMs idle.
+ *   q        : bf16 [B, h, n_q, d_k], 1 <= n_q <= 8.
+ *   k_cache, v_cache : bf16 [B, h, L_max, d_k]; rows past cache_lens[b] are
+ *              never used.
+ *   o, lse   : bf16 [B, h, n_q, d_k] and float [B, h, n_q] (lse may be NULL).
+ *   d_k      : 64 (else ATTN_ERR_UNSUPPORTED); B*h <= 65535.
+ *   cache_lens : device int32[B] (clamped to [0, L_max] on the device), or
+ *              NULL when every sequence fills the cache.
+ *   workspace, workspace_bytes : caller-owned device scratch of at least
+ *              attn_decode_workspace_bytes(...) bytes (16-byte aligned) for the
+ *              per-chunk partial results; may be NULL when that size is 0.
+ */
+int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                int B, int h, int n_q, int L_max, int d_k, float scale, const int* cache_lens,
+                void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
+/* Scratch bytes attn_decode needs for these sizes on the current device
+ * (0 when no split is needed, or for unsupported sizes). */
+size_t attn_decode_workspace_bytes(int B, int h, int n_q, int L_max, int d_k);
 
 /*
  * attn_check -- synchronise `stream`, then report (and clear) any error a

@@ -87,6 +87,23 @@ def test_unsupported_head_sizes(lib):
         assert _call(True, d=d) == UNS
 
 
+def test_decode_arguments_rejected_on_host(lib):
+    def call(q=A, k=A, v=A, o=A, lse=None, B=1, h=1, n_q=1, L=8, d=64, scale=0.125, lens=None,
+             ws=None, ws_bytes=0):
+        return binding.attn_decode_raw(q, k, v, o, lse, B, h, n_q, L, d, scale, lens, ws,
+                                       ws_bytes, None)
+    INV, UNS = binding.ATTN_ERR_INVALID_ARG, binding.ATTN_ERR_UNSUPPORTED
+    assert call(q=None) == INV
+    assert call(k=A + 4) == INV
+    assert call(n_q=0) == INV and call(L=0) == INV and call(B=0) == INV
+    assert call(scale=float("nan")) == INV
+    assert call(lens=A + 2) == INV
+    assert call(n_q=9) == UNS
+    assert call(d=32) == UNS
+    assert call(B=1 << 9, h=1 << 8) == UNS      # B*h beyond the grid's y extent
+    assert lib.attn_decode_workspace_bytes(1, 1, 9, 8, 64) == 0   # unsupported sizes
+
+
 def test_diag_entry_points_validate(lib):
     assert lib.attn_diag_tile(None, A, A, A, A, A, None) == binding.ATTN_ERR_INVALID_ARG
     assert lib.attn_diag_tile(A, A, A + 4, A, A, A, None) == binding.ATTN_ERR_INVALID_ARG

@@ -1,0 +1,120 @@
+"""GPU parity of the decoding path (a few new queries against a key/value
+cache) with the float64 oracle: the same operation as the fused forward with
+key padding, so the oracle is called with the cache lengths as key lengths.
+Tolerances as for the bf16 forward: max |dO| <= 2e-2, mean |dO| <= 2e-3,
+|dLSE| <= 1e-3 (this path keeps P in float32, so it lands far inside them).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from transformer_head_scaled_gb300 import binding, inputs
+from transformer_head_scaled_gb300.inputs import MASK_KEY_PADDING, MASK_NONE, Workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from transformer_head_scaled_gb300.build import build
+    build()
+    oracle.build()
+    return binding.load()
+
+
+def _check(o, lse, q, k, v, lens, scale):
+    mask = MASK_NONE if lens is None else MASK_KEY_PADDING
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, scale, mask, lens)
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    err = np.abs(o - o_ref)
+    assert np.isfinite(o).all()
+    assert err.max() <= 2e-2 and err.mean() <= 2e-3, (err.max(), err.mean())
+    assert np.array_equal(np.isneginf(lse), np.isneginf(l_ref))
+    fin = np.isfinite(l_ref)
+    if fin.any():
+        assert np.abs(lse[fin] - l_ref[fin]).max() <= 1e-3
+
+
+def _case(B, h, n_q, L_max, lens, seed=0):
+    w = Workload("dec", B, h, n_q, L_max, 64, MASK_KEY_PADDING, "bf16", kind="decode")
+    q, k, v, _ = inputs.make_inputs(w, device="cuda", seeds=(seed, seed + 1, seed + 2, seed + 3))
+    kl = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
+    return w, q, k, v, kl
+
+
+@pytest.mark.parametrize("n_q", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("shape", [(3, 2, 300), (2, 4, 1000), (1, 1, 1), (4, 3, 129), (1, 2, 4096)])
+def test_decode_matches_oracle(n_q, shape):
+    B, h, L = shape
+    lens = [max(0, (L * (b + 1)) // B - b) for b in range(B)]
+    w, q, k, v, kl = _case(B, h, n_q, L, lens)
+    o, lse = binding.attn_decode(q, k, v, kl, scale=w.scale)
+    binding.check()
+    _check(o, lse, q, k, v, kl, w.scale)
+
+
+def test_decode_tile_boundary_lengths_and_empty_cache():
+    lens = [0, 1, 127, 128, 129, 255, 256, 257, 511, 512]
+    w, q, k, v, kl = _case(len(lens), 2, 2, 512, lens)
+    o, lse = binding.attn_decode(q, k, v, kl, scale=w.scale)
+    binding.check()
+    _check(o, lse, q, k, v, kl, w.scale)
+
+
+def test_decode_split_and_unsplit_paths():
+    # few heads and a long cache: chunks merged by the second kernel
+    assert binding.decode_workspace_bytes(1, 2, 1, 4096) > 0
+    # many heads: one CTA per head, no workspace
+    assert binding.decode_workspace_bytes(128, 8, 1, 512) == 0
+    for B, h, L in ((1, 2, 4096), (128, 8, 512)):
+        lens = list(np.random.default_rng(B).integers(1, L + 1, size=B))
+        w, q, k, v, kl = _case(B, h, 1, L, lens, seed=5)
+        o, lse = binding.attn_decode(q, k, v, kl, scale=w.scale)
+        binding.check()
+        _check(o, lse, q, k, v, kl, w.scale)
+
+
+def test_decode_without_lengths_uses_whole_cache():
+    w, q, k, v, _ = _case(2, 3, 2, 700, None)
+    o, lse = binding.attn_decode(q, k, v, None, scale=w.scale)
+    binding.check()
+    _check(o, lse, q, k, v, None, w.scale)
+
+
+def test_decode_ignores_cache_past_lengths():
+    """Cache rows past the filled length may hold anything, NaN included."""
+    lens = [5, 300, 0, 129]
+    w, q, k, v, kl = _case(4, 2, 1, 512, lens)
+    o_ref, l_ref = binding.attn_decode(q, k, v, kl, scale=w.scale)
+    k2, v2 = k.clone(), v.clone()
+    for b, L in enumerate(lens):
+        k2[b, :, L:] = float("nan")
+        v2[b, :, L:] = float("nan")
+    o, lse = binding.attn_decode(q, k2, v2, kl, scale=w.scale)
+    binding.check()
+    assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
+def test_decode_rejects_short_workspace():
+    w, q, k, v, kl = _case(1, 2, 1, 4096, [4096])
+    need = binding.decode_workspace_bytes(1, 2, 1, 4096)
+    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    rc = binding.attn_decode_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), None,
+                                 1, 2, 1, 4096, 64, w.scale, kl.data_ptr(), ws.data_ptr(),
+                                 ws.numel(), torch.cuda.current_stream().cuda_stream)
+    assert rc == binding.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["decode_beam", "decode_long"])
+def test_decode_workloads_full(name):
+    """The decoding workloads the benchmark times, every output row."""
+    w = inputs.WORKLOADS[name]
+    q, k, v, kl = inputs.make_inputs(w, device="cuda")
+    o, lse = binding.attn_decode(q, k, v, kl, scale=w.scale)
+    binding.check()
+    _check(o, lse, q, k, v, kl, w.scale)

@@ -9,7 +9,8 @@ from .inputs import MASK_CAUSAL, MASK_KEY_PADDING, MASK_NONE  # noqa: F401
 
 
 def __getattr__(name):
-    if name in ("attn_fwd", "attn_fwd_f32", "attn_fwd_raw", "attn_fwd_f32_raw",
+    if name in ("attn_fwd", "attn_fwd_f32", "attn_fwd_raw", "attn_fwd_f32_raw", "attn_decode",
+                "decode_workspace_bytes",
                 "load", "AttnError", "status_string", "check"):
         from . import binding
         return getattr(binding, name)

@@ -26,7 +26,8 @@ ATTN_ERR_CUDA = -3
 ATTN_ERR_TIMEOUT = -4
 
 # Every entry point declared in include/attn.h.
-EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_check", "attn_status_string",
+EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_decode", "attn_decode_workspace_bytes",
+           "attn_check", "attn_status_string",
            "attn_last_cuda_error", "attn_set_wait_limit_ns", "attn_launch_count",
            "attn_diag_tile", "attn_diag_wait_timeout")
 
@@ -59,6 +60,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.restype = i32
             fn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, vp]
+        lib.attn_decode.restype = i32
+        lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp,
+                                    ctypes.c_size_t, vp]
+        lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         lib.attn_check.restype = i32
         lib.attn_check.argtypes = [vp]
         lib.attn_status_string.restype = ctypes.c_char_p
@@ -149,6 +155,53 @@ def attn_fwd_f32(q, k, v, **kw):
     if q.dtype != torch.float32:
         raise ValueError("attn_fwd_f32 takes float32 tensors")
     return attn_fwd(q, k, v, **kw)
+
+
+def decode_workspace_bytes(B: int, h: int, n_q: int, L_max: int, d: int = 64) -> int:
+    """Scratch bytes attn_decode needs on the current device (0: none)."""
+    return int(load().attn_decode_workspace_bytes(B, h, n_q, L_max, d))
+
+
+def attn_decode_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, L_max, d, scale,
+                    lens_ptr, ws_ptr, ws_bytes, stream_ptr) -> int:
+    """The C call itself, on raw device pointers; returns the status code."""
+    return load().attn_decode(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, L_max, d,
+                              float(scale), lens_ptr, ws_ptr, int(ws_bytes), stream_ptr)
+
+
+def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                cache_lens: torch.Tensor | None = None, scale: float | None = None,
+                out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                workspace: torch.Tensor | None = None, with_lse: bool = True, stream=None):
+    """n_q <= 8 new queries q [B,h,n_q,d] against bf16 caches [B,h,L_max,d];
+    query i sees the first cache_lens[b] keys (all L_max when None).
+    Returns (o, lse)."""
+    for t in (q, k_cache, v_cache):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError("q and the caches must be contiguous bf16 CUDA [B, h, n, d] tensors")
+    B, h, n_q, d = q.shape
+    L_max = k_cache.shape[2]
+    if tuple(k_cache.shape) != (B, h, L_max, d) or tuple(v_cache.shape) != (B, h, L_max, d):
+        raise ValueError("caches must be [B, h, L_max, d] with q's B, h, d")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if cache_lens is not None and (cache_lens.dtype != torch.int32 or not cache_lens.is_cuda
+                                   or cache_lens.numel() != B or not cache_lens.is_contiguous()):
+        raise ValueError("cache_lens must be a contiguous int32 CUDA tensor of B entries")
+    if out is None:
+        out = torch.empty((B, h, n_q, d), dtype=q.dtype, device=q.device)
+    if lse is None and with_lse:
+        lse = torch.empty((B, h, n_q), dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes(B, h, n_q, L_max, d)
+    if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = attn_decode_raw(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), B, h, n_q,
+                         L_max, d, scale, _ptr(cache_lens), _ptr(workspace), ws_bytes,
+                         _stream_ptr(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode")
+    return out, lse
 
 
 def check(stream=None) -> None:

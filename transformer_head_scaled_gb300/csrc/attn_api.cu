@@ -188,6 +188,40 @@ int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float
   return ATTN_OK;
 }
 
+size_t attn_decode_workspace_bytes(int B, int h, int n_q, int L_max, int d_k) {
+  if (B < 1 || h < 1 || n_q < 1 || n_q > kDecodeMaxQueries || L_max < 1 || d_k != 64) return 0;
+  DeviceInfo* di = nullptr;
+  if (device_info(&di) != ATTN_OK) return 0;
+  return decode_plan(B, h, n_q, L_max, di->num_sms).workspace_bytes;
+}
+
+int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                int B, int h, int n_q, int L_max, int d_k, float scale, const int* cache_lens,
+                void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
+  int rc = check_common(q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, scale,
+                        ATTN_MASK_NONE, nullptr, 2);
+  if (rc != ATTN_OK) return rc;
+  if (cache_lens && (reinterpret_cast<uintptr_t>(cache_lens) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (d_k != 64 || n_q > kDecodeMaxQueries) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * h > 65535) return ATTN_ERR_UNSUPPORTED;  // grid.y
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di)) != ATTN_OK) return rc;
+  const DecodePlan plan = decode_plan(B, h, n_q, L_max, di->num_sms);
+  if (plan.workspace_bytes > 0 &&
+      (workspace == nullptr || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)))
+    return ATTN_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * h;
+  CUtensorMap tmk, tmv;
+  if ((rc = encode_3d(&tmk, k_cache, d_k, L_max, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&tmv, v_cache, d_k, L_max, bh, 128)) != ATTN_OK) return rc;
+  DecodeProblem pb{q, k_cache, v_cache, o, lse, B, h, n_q, L_max, scale, cache_lens};
+  cudaError_t e = launch_decode(pb, tmk, tmv, plan, static_cast<float*>(workspace),
+                                make_ctx(*di, stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(plan.splits > 1 ? 2 : 1);
+  return ATTN_OK;
+}
+
 int attn_check(struct CUstream_st* stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e);

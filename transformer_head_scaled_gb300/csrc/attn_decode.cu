@@ -1,0 +1,345 @@
+// attn_decode.cu -- attention of a few new queries against a key/value cache
+// (the autoregressive decoding step of "Attention Is All You Need", §3.1 and
+// §6.1 on "Lire << Attention Is All You Need >>": the decoder produces one
+// symbol at a time; beam search keeps 4 hypotheses, each a sequence of its
+// own here).
+//
+// Same operation as the fused forward with key padding: query i of (b, h)
+// sees the keys j < cache_lens[b] of its cache; O and LSE as in eq. (1).
+// With n_q <= 8 the work is a matrix-vector product per head: the kernel is
+// bound by HBM bandwidth (every cached key and value is read once), so it
+// runs on the CUDA cores and spends its effort on keeping the loads in
+// flight: a 3-deep TMA ring of 128-key tiles per CTA, two CTAs per SM.
+//
+// When B*h alone does not fill the GPU, the cache of each head is split into
+// chunks processed by different CTAs; each writes a partial result (its own
+// running max m, sum l and unnormalised O, base 2) to a workspace, and a
+// second kernel merges the partials of a head (the same rescaling the online
+// softmax uses between tiles).  With one chunk per head the first kernel
+// writes O and LSE directly and no workspace is used.
+#include <cuda_bf16.h>
+
+#include "attn_internal.cuh"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int DK = 64;
+constexpr int KT = 128;          // keys per tile
+constexpr int DSTAGES = 3;       // K/V ring depth
+constexpr int NWARPS = 4;        // each warp takes 32 keys of every tile
+constexpr int THREADS = NWARPS * 32;
+constexpr uint32_t TILE_BYTES = KT * DK * 2;  // 16 KB
+constexpr float LN2 = 0.693147180559945309f;
+
+struct __align__(1024) DecSmem {
+  uint8_t k[DSTAGES][TILE_BYTES];
+  uint8_t v[DSTAGES][TILE_BYTES];
+  float q[kDecodeMaxQueries][DK];  // queries, pre-scaled by scale*log2(e)
+  float red[NWARPS][kDecodeMaxQueries][DK + 2];  // per-warp partials for the final merge
+  uint64_t full[DSTAGES], empty[DSTAGES];
+  int abort;
+};
+
+struct DecParams {
+  const __nv_bfloat16* q;
+  const int* cache_lens;  // may be null: every key of the cache is valid
+  __nv_bfloat16* o;
+  float* lse;
+  float* part;  // workspace: [B*h][splits][n_q][DK + 2] (m, l, O), or null
+  int H, n_q, L_max, splits, chunk;
+  float scale_log2;
+  uint64_t limit_ns;
+  int* status;
+};
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int NQ>
+__global__ void __launch_bounds__(THREADS, 2)
+    attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
+                             const __grid_constant__ CUtensorMap tmv, const DecParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  DecSmem& sm = *reinterpret_cast<DecSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x, bh = blockIdx.y, b = bh / p.H;
+  int L = p.L_max;
+  if (p.cache_lens != nullptr) L = min(max(__ldg(p.cache_lens + b), 0), p.L_max);
+  const int begin = split * p.chunk;
+  const int end = min(L, begin + p.chunk);
+  const int ntiles = end > begin ? (end - begin + KT - 1) / KT : 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < DSTAGES; ++i) {
+      mbar_init(smem_u32(&sm.full[i]), 1);
+      mbar_init(smem_u32(&sm.empty[i]), NWARPS);
+    }
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  for (int e = threadIdx.x; e < NQ * DK; e += THREADS) {
+    const float x = __bfloat162float(p.q[(static_cast<size_t>(bh) * NQ + e / DK) * DK + e % DK]);
+    sm.q[e / DK][e % DK] = x * p.scale_log2;
+  }
+  __syncthreads();
+  const volatile int* abort = &sm.abort;
+  const bool producer = threadIdx.x == 0;
+  if (producer) {
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+    for (int i = 0; i < DSTAGES && i < ntiles; ++i) {
+      mbar_arrive_expect_tx(smem_u32(&sm.full[i]), 2 * TILE_BYTES);
+      tma_load_3d(smem_u32(sm.k[i]), &tmk, smem_u32(&sm.full[i]), 0, begin + i * KT, bh);
+      tma_load_3d(smem_u32(sm.v[i]), &tmv, smem_u32(&sm.full[i]), 0, begin + i * KT, bh);
+    }
+  }
+
+  float m[NQ], l[NQ], o0[NQ], o1[NQ];  // this warp's running state per query
+#pragma unroll
+  for (int qi = 0; qi < NQ; ++qi) m[qi] = -INFINITY, l[qi] = 0.f, o0[qi] = 0.f, o1[qi] = 0.f;
+  bool ok = true;
+  const int r = warp * 32 + lane;  // this lane's key row inside a tile
+  for (int t = 0; t < ntiles && ok; ++t) {
+    const int slot = t % DSTAGES;
+    const uint32_t ph = (t / DSTAGES) & 1;
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.full[slot]), ph, p.limit_ns, abort));
+    if (!ok) break;
+    // ---- scores of key r for every query (K row r, 128-byte swizzle)
+    const uint8_t* krow = sm.k[slot] + r * 128;
+    float s[NQ];
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) s[qi] = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 w = *reinterpret_cast<const uint4*>(krow + ((c ^ (r & 7)) << 4));
+      const float kf[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                           bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+#pragma unroll
+      for (int qi = 0; qi < NQ; ++qi) {
+        const float4 qa = *reinterpret_cast<const float4*>(&sm.q[qi][c * 8]);
+        const float4 qb = *reinterpret_cast<const float4*>(&sm.q[qi][c * 8 + 4]);
+        s[qi] = fmaf(qa.x, kf[0], s[qi]);
+        s[qi] = fmaf(qa.y, kf[1], s[qi]);
+        s[qi] = fmaf(qa.z, kf[2], s[qi]);
+        s[qi] = fmaf(qa.w, kf[3], s[qi]);
+        s[qi] = fmaf(qb.x, kf[4], s[qi]);
+        s[qi] = fmaf(qb.y, kf[5], s[qi]);
+        s[qi] = fmaf(qb.z, kf[6], s[qi]);
+        s[qi] = fmaf(qb.w, kf[7], s[qi]);
+      }
+    }
+    const bool valid = begin + t * KT + r < end;
+    // ---- online softmax over this warp's 32 keys, then P V with V row j
+    float pr[NQ];
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) {
+      const float sv = valid ? s[qi] : -INFINITY;
+      const float mt = warp_max(sv);
+      const float mn = fmaxf(m[qi], mt);
+      const float base = mn == -INFINITY ? 0.f : mn;
+      const float alpha = ex2(m[qi] - base);  // 0 when m = -inf
+      l[qi] *= alpha;
+      o0[qi] *= alpha;
+      o1[qi] *= alpha;
+      m[qi] = mn;
+      pr[qi] = ex2(sv - base);  // 0 for invalid keys
+      l[qi] += pr[qi];          // per-lane partial sum, reduced at the end
+    }
+    // values of keys past the cache length are never used (not even times 0)
+    const int nvalid = min(32, max(0, end - (begin + t * KT + warp * 32)));
+#pragma unroll 4
+    for (int j = 0; j < nvalid; ++j) {
+      const int vr = warp * 32 + j;
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(
+          sm.v[slot] + vr * 128 + ((((lane >> 2) ^ (vr & 7)) << 4) | ((lane & 3) << 2)));
+      const float v0 = bf16lo(w), v1 = bf16hi(w);
+#pragma unroll
+      for (int qi = 0; qi < NQ; ++qi) {
+        const float pj = __shfl_sync(0xffffffffu, pr[qi], j);
+        o0[qi] = fmaf(pj, v0, o0[qi]);
+        o1[qi] = fmaf(pj, v1, o1[qi]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sm.empty[slot]));
+    // refill this slot with tile t + DSTAGES once every warp is done with it
+    if (producer && t + DSTAGES < ntiles) {
+      if (mbar_wait(smem_u32(&sm.empty[slot]), ph, p.limit_ns, abort)) {
+        mbar_arrive_expect_tx(smem_u32(&sm.full[slot]), 2 * TILE_BYTES);
+        tma_load_3d(smem_u32(sm.k[slot]), &tmk, smem_u32(&sm.full[slot]), 0,
+                    begin + (t + DSTAGES) * KT, bh);
+        tma_load_3d(smem_u32(sm.v[slot]), &tmv, smem_u32(&sm.full[slot]), 0,
+                    begin + (t + DSTAGES) * KT, bh);
+      } else {
+        atomicCAS(p.status, kDevOk, kDevTimeout);
+        *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+      }
+    }
+  }
+  if (!ok && lane == 0) {
+    atomicCAS(p.status, kDevOk, kDevTimeout);
+    *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+  }
+  // Copies still in flight land before shared memory goes away.
+  if (producer) {
+    const int never = 0;
+    for (int i = 0; i < DSTAGES && i < ntiles; ++i) {
+      const int last = i + ((ntiles - 1 - i) / DSTAGES) * DSTAGES;  // last tile issued to slot i
+      mbar_wait(smem_u32(&sm.full[i]), (last / DSTAGES) & 1, p.limit_ns, &never);
+    }
+  }
+
+  // ---- merge the four warps' states: lane sums, then across warps in smem
+#pragma unroll
+  for (int qi = 0; qi < NQ; ++qi) {
+    const float lw = warp_sum(l[qi]);
+    sm.red[warp][qi][2 * lane] = o0[qi];
+    sm.red[warp][qi][2 * lane + 1] = o1[qi];
+    if (lane == 0) {
+      sm.red[warp][qi][DK] = m[qi];
+      sm.red[warp][qi][DK + 1] = lw;
+    }
+  }
+  __syncthreads();
+  // warp qi % NWARPS writes query qi
+  for (int qi = warp; qi < NQ; qi += NWARPS) {
+    float mm = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) mm = fmaxf(mm, sm.red[w][qi][DK]);
+    const float base = mm == -INFINITY ? 0.f : mm;
+    float ll = 0.f, a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) {
+      const float f = ex2(sm.red[w][qi][DK] - base);
+      ll += f * sm.red[w][qi][DK + 1];
+      a0 += f * sm.red[w][qi][2 * lane];
+      a1 += f * sm.red[w][qi][2 * lane + 1];
+    }
+    const size_t row = static_cast<size_t>(bh) * NQ + qi;
+    if (p.splits == 1) {
+      const float inv = ll > 0.f ? 1.f / ll : 0.f;
+      reinterpret_cast<uint32_t*>(p.o + row * DK)[lane] = pack_bf16x2(a0 * inv, a1 * inv);
+      if (lane == 0 && p.lse != nullptr)
+        p.lse[row] = ll > 0.f ? (mm + __log2f(ll)) * LN2 : -INFINITY;
+    } else {
+      float* dst = p.part + ((static_cast<size_t>(bh) * p.splits + split) * NQ + qi) * (DK + 2);
+      dst[2 * lane] = a0;
+      dst[2 * lane + 1] = a1;
+      if (lane == 0) {
+        dst[DK] = mm;
+        dst[DK + 1] = ll;
+      }
+    }
+  }
+}
+
+// One warp per (b, h, query): merge the chunks' partial results.
+__global__ void __launch_bounds__(128)
+    attn_decode_combine_kernel(const float* __restrict__ part, __nv_bfloat16* __restrict__ o,
+                               float* __restrict__ lse, int rows, int n_q, int splits) {
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);  // (bh * n_q + qi)
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int bh = row / n_q, qi = row % n_q;
+  float mm = -INFINITY;
+  for (int sp = 0; sp < splits; ++sp)
+    mm = fmaxf(mm, part[((static_cast<size_t>(bh) * splits + sp) * n_q + qi) * (DK + 2) + DK]);
+  const float base = mm == -INFINITY ? 0.f : mm;
+  float ll = 0.f, a0 = 0.f, a1 = 0.f;
+  for (int sp = 0; sp < splits; ++sp) {
+    const float* src = part + ((static_cast<size_t>(bh) * splits + sp) * n_q + qi) * (DK + 2);
+    const float f = ex2(src[DK] - base);
+    ll += f * src[DK + 1];
+    a0 += f * src[2 * lane];
+    a1 += f * src[2 * lane + 1];
+  }
+  const float inv = ll > 0.f ? 1.f / ll : 0.f;
+  reinterpret_cast<uint32_t*>(o + static_cast<size_t>(row) * DK)[lane] =
+      pack_bf16x2(a0 * inv, a1 * inv);
+  if (lane == 0 && lse != nullptr) lse[row] = ll > 0.f ? (mm + __log2f(ll)) * LN2 : -INFINITY;
+}
+
+template <int NQ>
+cudaError_t launch_split(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecParams& p,
+                         int BH, cudaStream_t stream) {
+  const size_t smem = sizeof(DecSmem) + 1024;
+  cudaError_t err = cudaFuncSetAttribute(attn_decode_split_kernel<NQ>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  attn_decode_split_kernel<NQ><<<dim3(p.splits, BH), THREADS, smem, stream>>>(tmk, tmv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+DecodePlan decode_plan(int B, int H, int n_q, int L_max, int num_sms) {
+  DecodePlan plan;
+  const long long bh = static_cast<long long>(B) * H;
+  const int max_tiles = (L_max + KT - 1) / KT;
+  // about four CTAs per SM (two resident), and at least two tiles per chunk
+  const long long want = 4LL * num_sms;
+  int splits = bh >= want ? 1 : static_cast<int>((want + bh - 1) / bh);
+  splits = max(1, min(splits, max(1, max_tiles / 2)));
+  const int tiles_per = (max_tiles + splits - 1) / splits;
+  splits = (max_tiles + tiles_per - 1) / tiles_per;
+  plan.splits = splits;
+  plan.chunk = tiles_per * KT;
+  plan.workspace_bytes =
+      splits > 1 ? static_cast<size_t>(bh) * splits * n_q * (DK + 2) * sizeof(float) : 0;
+  return plan;
+}
+
+cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                          const DecodePlan& plan, float* workspace, const LaunchCtx& ctx) {
+  DecParams p;
+  p.q = static_cast<const __nv_bfloat16*>(pb.q);
+  p.cache_lens = pb.cache_lens;
+  p.o = static_cast<__nv_bfloat16*>(pb.o);
+  p.lse = pb.lse;
+  p.part = workspace;
+  p.H = pb.H;
+  p.n_q = pb.n_q;
+  p.L_max = pb.L_max;
+  p.splits = plan.splits;
+  p.chunk = plan.chunk;
+  p.scale_log2 = pb.scale * 1.4426950408889634f;
+  p.limit_ns = ctx.limit_ns;
+  p.status = ctx.status;
+  const int BH = pb.B * pb.H;
+  cudaError_t err;
+  switch (pb.n_q) {
+    case 1: err = launch_split<1>(tmk, tmv, p, BH, ctx.stream); break;
+    case 2: err = launch_split<2>(tmk, tmv, p, BH, ctx.stream); break;
+    case 3: err = launch_split<3>(tmk, tmv, p, BH, ctx.stream); break;
+    case 4: err = launch_split<4>(tmk, tmv, p, BH, ctx.stream); break;
+    case 5: err = launch_split<5>(tmk, tmv, p, BH, ctx.stream); break;
+    case 6: err = launch_split<6>(tmk, tmv, p, BH, ctx.stream); break;
+    case 7: err = launch_split<7>(tmk, tmv, p, BH, ctx.stream); break;
+    case 8: err = launch_split<8>(tmk, tmv, p, BH, ctx.stream); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (err != cudaSuccess || plan.splits == 1) return err;
+  const int rows = BH * pb.n_q;
+  attn_decode_combine_kernel<<<(rows + 3) / 4, 128, 0, ctx.stream>>>(
+      workspace, p.o, p.lse, rows, pb.n_q, plan.splits);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

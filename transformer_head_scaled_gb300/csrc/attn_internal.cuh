@@ -43,6 +43,33 @@ size_t fwd_tc_smem_bytes();
 // fp32 SIMT path (d in {16, 32, 64, 128}).
 cudaError_t launch_fwd_f32(const Problem& pb, const LaunchCtx& ctx);
 
+// Decode path (n_q <= kDecodeMaxQueries new queries against a cache).
+constexpr int kDecodeMaxQueries = 8;
+
+struct DecodeProblem {
+  const void* q;        // bf16 [B, H, n_q, 64]
+  const void* k_cache;  // bf16 [B, H, L_max, 64]
+  const void* v_cache;
+  void* o;              // bf16 [B, H, n_q, 64]
+  float* lse;           // [B, H, n_q] or null
+  int B, H, n_q, L_max;
+  float scale;
+  const int* cache_lens;  // device int32[B] or null (all L_max valid)
+};
+
+// How the cache of each head is split across CTAs; workspace_bytes = 0 when
+// one CTA per head suffices.
+struct DecodePlan {
+  int splits;
+  int chunk;  // keys per split, a multiple of the 128-key tile
+  size_t workspace_bytes;
+};
+DecodePlan decode_plan(int B, int H, int n_q, int L_max, int num_sms);
+// tmk / tmv describe the caches as 3-D (64, L_max, B*H) bf16 with a
+// (64, 128, 1) box and 128-byte swizzle; workspace holds plan.workspace_bytes.
+cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                          const DecodePlan& plan, float* workspace, const LaunchCtx& ctx);
+
 // Diagnostics.  The tensor maps are 2-D (64, 128) bf16, one box each.
 cudaError_t launch_diag_tile(const CUtensorMap& tmq, const CUtensorMap& tmk,
                              const CUtensorMap& tmv, const void* p, float* s, float* o,

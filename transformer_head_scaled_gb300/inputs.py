@@ -15,7 +15,8 @@ available here; these tensors stand in for them):
   Unit-variance q and k are the premise of the scaling argument in section
   3.2.1 (footnote: q.k then has mean 0 and variance d_k).
 * Per-sequence key lengths for encoder-decoder attention are integers uniform
-  on [64, n_k] inclusive, PCG64 seeded 3.
+  on [64, n_k] inclusive, PCG64 seeded 3 (decoding workloads: the filled part
+  of each key/value cache, uniform on [lens_lo, n_k]).
 * Layout is [B, h, n, d] contiguous (heads split as (h, seq, d)).
 """
 from __future__ import annotations
@@ -46,6 +47,7 @@ class Workload:
     mask: int
     dtype: str  # "bf16" or "f32"
     lens_lo: int = 64
+    kind: str = "fwd"  # "fwd": fused forward; "decode": few queries against a cache
     note: str = field(default="", compare=False)
 
     @property
@@ -70,6 +72,16 @@ WORKLOADS = {
                     note="big model, long sequence, unmasked"),
     "big_causal": Workload("big_causal", 8, 16, 4096, 4096, 64, MASK_CAUSAL,
                            "bf16", note="big model, long sequence, causal"),
+    # Decoding steps (section 6.1 on "Lire << Attention Is All You Need >>":
+    # beam search of width 4): one new query per hypothesis against its
+    # key/value cache; n_k is the cache capacity, the key lengths the filled
+    # part.
+    "decode_beam": Workload("decode_beam", 256, 8, 1, 512, 64, MASK_KEY_PADDING, "bf16",
+                            lens_lo=64, kind="decode",
+                            note="base model, 64 sentences x beam 4, cache up to 512"),
+    "decode_long": Workload("decode_long", 32, 16, 1, 4096, 64, MASK_KEY_PADDING, "bf16",
+                            lens_lo=2048, kind="decode",
+                            note="big model, 8 sentences x beam 4, cache up to 4096"),
 }
 
 
@@ -126,10 +138,15 @@ def algorithmic_flops(w: Workload, key_lens=None) -> float:
     return flops(w)
 
 
-def hbm_bytes(w: Workload) -> float:
+def hbm_bytes(w: Workload, key_lens=None) -> float:
     """Compulsory HBM bytes of one forward pass: Q, K, V read once, O written
-    once, LSE (float32) written once; the n_q x n_k scores never leave the chip."""
+    once, LSE (float32) written once; the n_q x n_k scores never leave the chip.
+    For a decoding step only the filled part of the caches is read."""
     es = 2 if w.dtype == "bf16" else 4
     qo = 2 * w.B * w.h * w.n_q * w.d * es
-    kv = 2 * w.B * w.h * w.n_k * w.d * es
+    if w.kind == "decode" and key_lens is not None:
+        lens = np.asarray(key_lens.cpu() if hasattr(key_lens, "cpu") else key_lens)
+        kv = 2 * w.h * float(np.minimum(lens, w.n_k).sum()) * w.d * es
+    else:
+        kv = 2 * w.B * w.h * w.n_k * w.d * es
     return float(qo + kv + 4 * w.B * w.h * w.n_q)
