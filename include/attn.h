@@ -53,7 +53,8 @@ typedef enum {
   ATTN_ERR_INVALID_ARG = -1, /* null/misaligned pointer, size < 1, bad mask or scale */
   ATTN_ERR_UNSUPPORTED = -2, /* head size or device this build does not cover */
   ATTN_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed, see attn_last_cuda_error */
-  ATTN_ERR_TIMEOUT = -4      /* a kernel gave up on a bounded wait (see attn_check) */
+  ATTN_ERR_TIMEOUT = -4,     /* a kernel gave up on a bounded wait (see attn_check) */
+  ATTN_ERR_SCRATCH_TOO_SMALL = -5 /* attn_decode_noalloc: sizes need more than its fixed scratch */
 } attn_status;
 
 /*
@@ -108,6 +109,37 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o
 /* Scratch bytes attn_decode needs for these sizes on the current device
  * (0 when no split is needed, or for unsupported sizes). */
 size_t attn_decode_workspace_bytes(int B, int h, int n_q, int L_max, int d_k);
+
+/* Size of the fixed scratch array behind attn_decode_noalloc (1 MiB). */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/*
+ * attn_decode_noalloc -- attn_decode without the workspace argument, for
+ * callers that cannot allocate device memory on the call path: an engine
+ * that plans all of its device memory ahead and allows no allocation while
+ * it serves requests, a plug-in that is handed only its input and output
+ * buffers, or a caller for whom the device-wide synchronisation an
+ * allocation may cause is not acceptable.  (This entry point has no
+ * counterpart in the paper; it only changes where the scratch lives.)
+ *
+ * The per-chunk partial results go to an array of
+ * ATTN_DECODE_NOALLOC_SCRATCH_BYTES that the library declares in its own
+ * device memory: every device that loads the library holds it until the
+ * process exits, and nothing is allocated or freed per call.  Sizes whose
+ * partials would not fit return ATTN_ERR_SCRATCH_TOO_SMALL (use attn_decode
+ * with a workspace of attn_decode_workspace_bytes(...) instead).
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and it keeps whatever the last call
+ * left in it; nothing in it needs to start at zero (every partial is written
+ * before it is read).  Calls whose kernels may overlap on the GPU (different
+ * streams, or host threads on the same device) race on the array: order them
+ * on one stream.  Arguments and results otherwise as attn_decode.
+ */
+int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o,
+                        float* lse, int B, int h, int n_q, int L_max, int d_k, float scale,
+                        const int* cache_lens, struct CUstream_st* stream);
 
 /*
  * attn_check -- synchronise `stream`, then report (and clear) any error a

@@ -24,9 +24,12 @@ ATTN_ERR_INVALID_ARG = -1
 ATTN_ERR_UNSUPPORTED = -2
 ATTN_ERR_CUDA = -3
 ATTN_ERR_TIMEOUT = -4
+ATTN_ERR_SCRATCH_TOO_SMALL = -5
+DECODE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 # Every entry point declared in include/attn.h.
 EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_decode", "attn_decode_workspace_bytes",
+           "attn_decode_noalloc",
            "attn_check", "attn_status_string",
            "attn_last_cuda_error", "attn_set_wait_limit_ns", "attn_launch_count",
            "attn_diag_tile", "attn_diag_wait_timeout")
@@ -63,6 +66,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_decode.restype = i32
         lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp,
                                     ctypes.c_size_t, vp]
+        lib.attn_decode_noalloc.restype = i32
+        lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp,
+                                            vp]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         lib.attn_check.restype = i32

@@ -133,6 +133,32 @@ int encode_2d(CUtensorMap* map, const void* base) {
   return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
 }
 
+// Scratch for attn_decode_noalloc: a fixed-size array in the library's own
+// device memory, created when the library's module is loaded on a device and
+// kept until the process exits.  Host code only knows the symbol; the device
+// address is looked up once per device (scratch_on_device) and handed to the
+// kernels as a plain pointer.
+static __device__ __align__(256) unsigned char g_decode_scratch[ATTN_DECODE_NOALLOC_SCRATCH_BYTES];
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_decode_scratch on the current device (looked up on the
+// first call per device, under the set-up lock).
+int scratch_on_device(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* addr = nullptr;
+    if ((e = cudaGetSymbolAddress(&addr, g_decode_scratch)) != cudaSuccess) return cuda_fail(e);
+    if (addr == nullptr) return cuda_fail(cudaErrorInvalidSymbol);
+    g_scratch_addr[dev] = addr;
+  }
+  *out = g_scratch_addr[dev];
+  return ATTN_OK;
+}
+
 LaunchCtx make_ctx(const DeviceInfo& di, cudaStream_t stream) {
   LaunchCtx ctx;
   ctx.num_sms = di.num_sms;
@@ -222,6 +248,33 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o
   return ATTN_OK;
 }
 
+int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o,
+                        float* lse, int B, int h, int n_q, int L_max, int d_k, float scale,
+                        const int* cache_lens, struct CUstream_st* stream) {
+  int rc = check_common(q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, scale,
+                        ATTN_MASK_NONE, nullptr, 2);
+  if (rc != ATTN_OK) return rc;
+  if (cache_lens && (reinterpret_cast<uintptr_t>(cache_lens) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (d_k != 64 || n_q > kDecodeMaxQueries) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * h > 65535) return ATTN_ERR_UNSUPPORTED;  // grid.y
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di)) != ATTN_OK) return rc;
+  const DecodePlan plan = decode_plan(B, h, n_q, L_max, di->num_sms);
+  if (plan.workspace_bytes > ATTN_DECODE_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_SCRATCH_TOO_SMALL;
+  void* scratch = nullptr;
+  if ((rc = scratch_on_device(&scratch)) != ATTN_OK) return rc;
+  const long long bh = static_cast<long long>(B) * h;
+  CUtensorMap tmk, tmv;
+  if ((rc = encode_3d(&tmk, k_cache, d_k, L_max, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&tmv, v_cache, d_k, L_max, bh, 128)) != ATTN_OK) return rc;
+  DecodeProblem pb{q, k_cache, v_cache, o, lse, B, h, n_q, L_max, scale, cache_lens};
+  cudaError_t e = launch_decode(pb, tmk, tmv, plan, static_cast<float*>(scratch),
+                                make_ctx(*di, stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(plan.splits > 1 ? 2 : 1);
+  return ATTN_OK;
+}
+
 int attn_check(struct CUstream_st* stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -245,6 +298,8 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_UNSUPPORTED: return "unsupported head size or device";
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_TIMEOUT: return "a bounded wait inside a kernel timed out";
+    case ATTN_ERR_SCRATCH_TOO_SMALL:
+      return "these sizes need more scratch than the library's fixed scratch array holds";
     default: return "unknown status";
   }
 }
