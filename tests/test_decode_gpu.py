@@ -68,9 +68,9 @@ def test_decode_tile_boundary_lengths_and_empty_cache():
 def test_decode_split_and_unsplit_paths():
     # few heads and a long cache: chunks merged by the second kernel
     assert binding.decode_workspace_bytes(1, 2, 1, 4096) > 0
-    # many heads: one CTA per head, no workspace
-    assert binding.decode_workspace_bytes(128, 8, 1, 512) == 0
-    for B, h, L in ((1, 2, 4096), (128, 8, 512)):
+    # many heads: one unit per head, no workspace
+    assert binding.decode_workspace_bytes(256, 8, 1, 512) == 0
+    for B, h, L in ((1, 2, 4096), (256, 8, 512)):
         lens = list(np.random.default_rng(B).integers(1, L + 1, size=B))
         w, q, k, v, kl = _case(B, h, 1, L, lens, seed=5)
         o, lse = binding.attn_decode(q, k, v, kl, scale=w.scale)

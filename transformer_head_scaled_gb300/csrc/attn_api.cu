@@ -159,6 +159,17 @@ int scratch_on_device(void** out) {
   return ATTN_OK;
 }
 
+// K and V caches with 128-key boxes, then with 32-key boxes for partial tiles.
+int encode_decode_maps(CUtensorMap* maps, const void* k_cache, const void* v_cache, int d_k,
+                       int L_max, int B, int h) {
+  const long long bh = static_cast<long long>(B) * h;
+  int rc;
+  if ((rc = encode_3d(&maps[0], k_cache, d_k, L_max, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&maps[1], v_cache, d_k, L_max, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&maps[2], k_cache, d_k, L_max, bh, 32)) != ATTN_OK) return rc;
+  return encode_3d(&maps[3], v_cache, d_k, L_max, bh, 32);
+}
+
 LaunchCtx make_ctx(const DeviceInfo& di, cudaStream_t stream) {
   LaunchCtx ctx;
   ctx.num_sms = di.num_sms;
@@ -236,12 +247,10 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o
   if (plan.workspace_bytes > 0 &&
       (workspace == nullptr || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)))
     return ATTN_ERR_INVALID_ARG;
-  const long long bh = static_cast<long long>(B) * h;
-  CUtensorMap tmk, tmv;
-  if ((rc = encode_3d(&tmk, k_cache, d_k, L_max, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&tmv, v_cache, d_k, L_max, bh, 128)) != ATTN_OK) return rc;
+  CUtensorMap maps[4];
+  if ((rc = encode_decode_maps(maps, k_cache, v_cache, d_k, L_max, B, h)) != ATTN_OK) return rc;
   DecodeProblem pb{q, k_cache, v_cache, o, lse, B, h, n_q, L_max, scale, cache_lens};
-  cudaError_t e = launch_decode(pb, tmk, tmv, plan, static_cast<float*>(workspace),
+  cudaError_t e = launch_decode(pb, maps, plan, static_cast<float*>(workspace),
                                 make_ctx(*di, stream));
   if (e != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(plan.splits > 1 ? 2 : 1);
@@ -263,12 +272,10 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
   if (plan.workspace_bytes > ATTN_DECODE_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_SCRATCH_TOO_SMALL;
   void* scratch = nullptr;
   if ((rc = scratch_on_device(&scratch)) != ATTN_OK) return rc;
-  const long long bh = static_cast<long long>(B) * h;
-  CUtensorMap tmk, tmv;
-  if ((rc = encode_3d(&tmk, k_cache, d_k, L_max, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&tmv, v_cache, d_k, L_max, bh, 128)) != ATTN_OK) return rc;
+  CUtensorMap maps[4];
+  if ((rc = encode_decode_maps(maps, k_cache, v_cache, d_k, L_max, B, h)) != ATTN_OK) return rc;
   DecodeProblem pb{q, k_cache, v_cache, o, lse, B, h, n_q, L_max, scale, cache_lens};
-  cudaError_t e = launch_decode(pb, tmk, tmv, plan, static_cast<float*>(scratch),
+  cudaError_t e = launch_decode(pb, maps, plan, static_cast<float*>(scratch),
                                 make_ctx(*di, stream));
   if (e != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(plan.splits > 1 ? 2 : 1);

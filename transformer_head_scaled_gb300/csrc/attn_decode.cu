@@ -9,7 +9,8 @@
 // With n_q <= 8 the work is a matrix-vector product per head: the kernel is
 // bound by HBM bandwidth (every cached key and value is read once), so it
 // runs on the CUDA cores and spends its effort on keeping the loads in
-// flight: a 3-deep TMA ring of 128-key tiles per CTA, two CTAs per SM.
+// flight: a 2-deep TMA ring of 128-key tiles per CTA, three persistent CTAs
+// per SM, the ring running ahead across the heads a CTA processes.
 //
 // When B*h alone does not fill the GPU, the cache of each head is split into
 // chunks processed by different CTAs; each writes a partial result (its own
@@ -29,17 +30,21 @@ using namespace ptx;
 
 constexpr int DK = 64;
 constexpr int KT = 128;          // keys per tile
-constexpr int DSTAGES = 3;       // K/V ring depth
+constexpr int DSTAGES = 2;       // K/V ring depth (three CTAs per SM keep 6 tiles in flight)
 constexpr int NWARPS = 4;        // each warp takes 32 keys of every tile
 constexpr int THREADS = NWARPS * 32;
 constexpr uint32_t TILE_BYTES = KT * DK * 2;  // 16 KB
+constexpr int TAIL = 32;                        // keys per box of a partial last tile
+constexpr uint32_t TAIL_BYTES = TAIL * DK * 2;  // 4 KB (a multiple of the 1 KB swizzle atom)
 constexpr float LN2 = 0.693147180559945309f;
 
 struct __align__(1024) DecSmem {
   uint8_t k[DSTAGES][TILE_BYTES];
   uint8_t v[DSTAGES][TILE_BYTES];
-  float q[kDecodeMaxQueries][DK];  // queries, pre-scaled by scale*log2(e)
-  float red[NWARPS][kDecodeMaxQueries][DK + 2];  // per-warp partials for the final merge
+  union {
+    float q[kDecodeMaxQueries][DK];                // queries, pre-scaled by scale*log2(e)
+    float red[NWARPS][kDecodeMaxQueries][DK + 2];  // per-warp partials, after the tiles
+  };
   uint64_t full[DSTAGES], empty[DSTAGES];
   int abort;
 };
@@ -50,7 +55,7 @@ struct DecParams {
   __nv_bfloat16* o;
   float* lse;
   float* part;  // workspace: [B*h][splits][n_q][DK + 2] (m, l, O), or null
-  int H, n_q, L_max, splits, chunk;
+  int H, BH, n_q, L_max, splits, chunk;
   float scale_log2;
   uint64_t limit_ns;
   int* status;
@@ -70,20 +75,29 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Persistent: CTA c processes the work units c, c + gridDim.x, ... (a unit
+// is one chunk of one head's cache); thread 0 keeps the TMA ring DSTAGES
+// tiles ahead across unit boundaries, so the next head's first tiles are in
+// flight while the current one is finished.
 template <int NQ>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(THREADS, 3)
     attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
-                             const __grid_constant__ CUtensorMap tmv, const DecParams p) {
+                             const __grid_constant__ CUtensorMap tmv,
+                             const __grid_constant__ CUtensorMap tmk_tail,
+                             const __grid_constant__ CUtensorMap tmv_tail, const DecParams p) {
   extern __shared__ uint8_t smem_raw[];
   DecSmem& sm = *reinterpret_cast<DecSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x, bh = blockIdx.y, b = bh / p.H;
-  int L = p.L_max;
-  if (p.cache_lens != nullptr) L = min(max(__ldg(p.cache_lens + b), 0), p.L_max);
-  const int begin = split * p.chunk;
-  const int end = min(L, begin + p.chunk);
-  const int ntiles = end > begin ? (end - begin + KT - 1) / KT : 0;
+  const int units = p.BH * p.splits;
+  // keys [begin, end) of unit u's chunk
+  auto unit_keys = [&](int u, int& bh, int& begin, int& end) {
+    bh = u / p.splits;
+    int L = p.L_max;
+    if (p.cache_lens != nullptr) L = min(max(__ldg(p.cache_lens + bh / p.H), 0), p.L_max);
+    begin = (u % p.splits) * p.chunk;
+    end = min(L, begin + p.chunk);
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < DSTAGES; ++i) {
@@ -93,158 +107,230 @@ __global__ void __launch_bounds__(THREADS, 2)
     sm.abort = 0;
     fence_mbar_init();
   }
-  for (int e = threadIdx.x; e < NQ * DK; e += THREADS) {
-    const float x = __bfloat162float(p.q[(static_cast<size_t>(bh) * NQ + e / DK) * DK + e % DK]);
-    sm.q[e / DK][e % DK] = x * p.scale_log2;
-  }
   __syncthreads();
   const volatile int* abort = &sm.abort;
   const bool producer = threadIdx.x == 0;
+
+  // ---- producer state (thread 0): the next (unit, tile) to load
+  int pu = blockIdx.x, pt = 0, pbh = 0, pbegin = 0, pend = 0;
+  if (producer && pu < units) unit_keys(pu, pbh, pbegin, pend);
+  uint32_t issued = 0;
+  bool pok = true;
+  auto produce_one = [&]() {
+    while (pu < units && pbegin + pt * KT >= pend) {
+      pu += gridDim.x;
+      pt = 0;
+      if (pu < units) unit_keys(pu, pbh, pbegin, pend);
+    }
+    if (pu >= units || !pok) return;
+    const uint32_t slot = issued % DSTAGES;
+    if (issued >= DSTAGES &&
+        !mbar_wait(smem_u32(&sm.empty[slot]), ((issued / DSTAGES) - 1) & 1, p.limit_ns, abort)) {
+      pok = false;
+      return;
+    }
+    const int key0 = pbegin + pt * KT;
+    const int rem = pend - key0;
+    const uint32_t bar = smem_u32(&sm.full[slot]);
+    if (rem >= KT) {
+      mbar_arrive_expect_tx(bar, 2 * TILE_BYTES);
+      tma_load_3d(smem_u32(sm.k[slot]), &tmk, bar, 0, key0, pbh);
+      tma_load_3d(smem_u32(sm.v[slot]), &tmv, bar, 0, key0, pbh);
+    } else {
+      // a partial last tile: only the 32-key boxes that hold valid keys (the
+      // rows after them keep stale data, which the consumers never use)
+      const int nbox = (rem + TAIL - 1) / TAIL;
+      mbar_arrive_expect_tx(bar, 2 * nbox * TAIL_BYTES);
+      for (int i = 0; i < nbox; ++i) {
+        tma_load_3d(smem_u32(sm.k[slot]) + i * TAIL_BYTES, &tmk_tail, bar, 0, key0 + i * TAIL, pbh);
+        tma_load_3d(smem_u32(sm.v[slot]) + i * TAIL_BYTES, &tmv_tail, bar, 0, key0 + i * TAIL, pbh);
+      }
+    }
+    ++pt;
+    ++issued;
+  };
   if (producer) {
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
-    for (int i = 0; i < DSTAGES && i < ntiles; ++i) {
-      mbar_arrive_expect_tx(smem_u32(&sm.full[i]), 2 * TILE_BYTES);
-      tma_load_3d(smem_u32(sm.k[i]), &tmk, smem_u32(&sm.full[i]), 0, begin + i * KT, bh);
-      tma_load_3d(smem_u32(sm.v[i]), &tmv, smem_u32(&sm.full[i]), 0, begin + i * KT, bh);
-    }
+    prefetch_tmap(&tmk_tail);
+    prefetch_tmap(&tmv_tail);
+    for (int i = 0; i < DSTAGES; ++i) produce_one();
   }
 
-  float m[NQ], l[NQ], o0[NQ], o1[NQ];  // this warp's running state per query
+  constexpr int QPT = (NQ * DK + THREADS - 1) / THREADS;  // query values per thread
+  auto load_q = [&](int u, float (&qv)[QPT]) {
+    const int bh = u / p.splits;
 #pragma unroll
-  for (int qi = 0; qi < NQ; ++qi) m[qi] = -INFINITY, l[qi] = 0.f, o0[qi] = 0.f, o1[qi] = 0.f;
+    for (int i = 0; i < QPT; ++i) {
+      const int e = threadIdx.x + i * THREADS;
+      qv[i] = (u < units && e < NQ * DK)
+                  ? __bfloat162float(p.q[(static_cast<size_t>(bh) * NQ + e / DK) * DK + e % DK])
+                  : 0.f;
+    }
+  };
+  float qv[QPT];
+  load_q(blockIdx.x, qv);
+
+  uint32_t consumed = 0;
   bool ok = true;
   const int r = warp * 32 + lane;  // this lane's key row inside a tile
-  for (int t = 0; t < ntiles && ok; ++t) {
-    const int slot = t % DSTAGES;
-    const uint32_t ph = (t / DSTAGES) & 1;
-    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.full[slot]), ph, p.limit_ns, abort));
-    if (!ok) break;
-    // ---- scores of key r for every query (K row r, 128-byte swizzle)
-    const uint8_t* krow = sm.k[slot] + r * 128;
-    float s[NQ];
+  for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    int bh, begin, end;
+    unit_keys(u, bh, begin, end);
+    const int ntiles = end > begin ? (end - begin + KT - 1) / KT : 0;
+    __syncthreads();  // the previous unit's merge has read sm.red and sm.q
 #pragma unroll
-    for (int qi = 0; qi < NQ; ++qi) s[qi] = 0.f;
+    for (int i = 0; i < QPT; ++i) {
+      const int e = threadIdx.x + i * THREADS;
+      if (e < NQ * DK) sm.q[e / DK][e % DK] = qv[i] * p.scale_log2;
+    }
+    __syncthreads();
+    load_q(u + gridDim.x, qv);  // the next unit's queries, consumed after this unit
+
+    float m[NQ], l[NQ], o0[NQ], o1[NQ];  // this warp's running state per query
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 w = *reinterpret_cast<const uint4*>(krow + ((c ^ (r & 7)) << 4));
-      const float kf[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
-                           bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+    for (int qi = 0; qi < NQ; ++qi) m[qi] = -INFINITY, l[qi] = 0.f, o0[qi] = 0.f, o1[qi] = 0.f;
+    for (int t = 0; t < ntiles; ++t, ++consumed) {
+      const int slot = consumed % DSTAGES;
+      const uint32_t ph = (consumed / DSTAGES) & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.full[slot]), ph, p.limit_ns, abort));
+      if (!ok) break;
+      // ---- scores of key r for every query (K row r, 128-byte swizzle)
+      // four independent partial sums per query (short dependency chains)
+      const uint8_t* krow = sm.k[slot] + r * 128;
+      float s[NQ], s1[NQ], s2[NQ], s3[NQ];
+#pragma unroll
+      for (int qi = 0; qi < NQ; ++qi) s[qi] = s1[qi] = s2[qi] = s3[qi] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4*>(krow + ((c ^ (r & 7)) << 4));
+        const float kf[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                             bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi) {
+          const float4 qa = *reinterpret_cast<const float4*>(&sm.q[qi][c * 8]);
+          const float4 qb = *reinterpret_cast<const float4*>(&sm.q[qi][c * 8 + 4]);
+          s[qi] = fmaf(qa.x, kf[0], s[qi]);
+          s1[qi] = fmaf(qa.y, kf[1], s1[qi]);
+          s2[qi] = fmaf(qa.z, kf[2], s2[qi]);
+          s3[qi] = fmaf(qa.w, kf[3], s3[qi]);
+          s[qi] = fmaf(qb.x, kf[4], s[qi]);
+          s1[qi] = fmaf(qb.y, kf[5], s1[qi]);
+          s2[qi] = fmaf(qb.z, kf[6], s2[qi]);
+          s3[qi] = fmaf(qb.w, kf[7], s3[qi]);
+        }
+      }
+#pragma unroll
+      for (int qi = 0; qi < NQ; ++qi) s[qi] = (s[qi] + s1[qi]) + (s2[qi] + s3[qi]);
+      const bool valid = begin + t * KT + r < end;
+      // ---- online softmax over this warp's 32 keys, then P V with V row j
+      float pr[NQ];
 #pragma unroll
       for (int qi = 0; qi < NQ; ++qi) {
-        const float4 qa = *reinterpret_cast<const float4*>(&sm.q[qi][c * 8]);
-        const float4 qb = *reinterpret_cast<const float4*>(&sm.q[qi][c * 8 + 4]);
-        s[qi] = fmaf(qa.x, kf[0], s[qi]);
-        s[qi] = fmaf(qa.y, kf[1], s[qi]);
-        s[qi] = fmaf(qa.z, kf[2], s[qi]);
-        s[qi] = fmaf(qa.w, kf[3], s[qi]);
-        s[qi] = fmaf(qb.x, kf[4], s[qi]);
-        s[qi] = fmaf(qb.y, kf[5], s[qi]);
-        s[qi] = fmaf(qb.z, kf[6], s[qi]);
-        s[qi] = fmaf(qb.w, kf[7], s[qi]);
+        const float sv = valid ? s[qi] : -INFINITY;
+        const float mt = warp_max(sv);
+        const float mn = fmaxf(m[qi], mt);
+        const float base = mn == -INFINITY ? 0.f : mn;
+        const float alpha = ex2(m[qi] - base);  // 0 when m = -inf
+        l[qi] *= alpha;
+        o0[qi] *= alpha;
+        o1[qi] *= alpha;
+        m[qi] = mn;
+        pr[qi] = ex2(sv - base);  // 0 for invalid keys
+        l[qi] += pr[qi];          // per-lane partial sum, reduced at the end
       }
+      // values of keys past the cache length are never used (not even times
+      // 0); even and odd keys accumulate separately (shorter chains)
+      const int nvalid = min(32, max(0, end - (begin + t * KT + warp * 32)));
+      float e0[NQ], e1[NQ];
+#pragma unroll
+      for (int qi = 0; qi < NQ; ++qi) e0[qi] = e1[qi] = 0.f;
+#pragma unroll 4
+      for (int j = 0; j < nvalid; j += 2) {
+        const int vr = warp * 32 + j;
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(
+            sm.v[slot] + vr * 128 + ((((lane >> 2) ^ (vr & 7)) << 4) | ((lane & 3) << 2)));
+        const bool has2 = j + 1 < nvalid;
+        const uint32_t w2 = has2 ? *reinterpret_cast<const uint32_t*>(
+                                       sm.v[slot] + (vr + 1) * 128 +
+                                       ((((lane >> 2) ^ ((vr + 1) & 7)) << 4) | ((lane & 3) << 2)))
+                                 : 0u;
+        const float v0 = bf16lo(w), v1 = bf16hi(w), u0 = bf16lo(w2), u1 = bf16hi(w2);
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi) {
+          const float pj = __shfl_sync(0xffffffffu, pr[qi], j);
+          const float pk = __shfl_sync(0xffffffffu, pr[qi], (j + 1) & 31);
+          o0[qi] = fmaf(pj, v0, o0[qi]);
+          o1[qi] = fmaf(pj, v1, o1[qi]);
+          e0[qi] = fmaf(has2 ? pk : 0.f, u0, e0[qi]);
+          e1[qi] = fmaf(has2 ? pk : 0.f, u1, e1[qi]);
+        }
+      }
+#pragma unroll
+      for (int qi = 0; qi < NQ; ++qi) o0[qi] += e0[qi], o1[qi] += e1[qi];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.empty[slot]));
+      if (producer) produce_one();  // refill the ring (possibly from the next unit)
     }
-    const bool valid = begin + t * KT + r < end;
-    // ---- online softmax over this warp's 32 keys, then P V with V row j
-    float pr[NQ];
+    if (!ok) break;
+
+    // ---- merge the four warps' states: lane sums, then across warps in smem
+    // (sm.red shares its space with sm.q: every warp is done with q first)
+    __syncthreads();
 #pragma unroll
     for (int qi = 0; qi < NQ; ++qi) {
-      const float sv = valid ? s[qi] : -INFINITY;
-      const float mt = warp_max(sv);
-      const float mn = fmaxf(m[qi], mt);
-      const float base = mn == -INFINITY ? 0.f : mn;
-      const float alpha = ex2(m[qi] - base);  // 0 when m = -inf
-      l[qi] *= alpha;
-      o0[qi] *= alpha;
-      o1[qi] *= alpha;
-      m[qi] = mn;
-      pr[qi] = ex2(sv - base);  // 0 for invalid keys
-      l[qi] += pr[qi];          // per-lane partial sum, reduced at the end
-    }
-    // values of keys past the cache length are never used (not even times 0)
-    const int nvalid = min(32, max(0, end - (begin + t * KT + warp * 32)));
-#pragma unroll 4
-    for (int j = 0; j < nvalid; ++j) {
-      const int vr = warp * 32 + j;
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(
-          sm.v[slot] + vr * 128 + ((((lane >> 2) ^ (vr & 7)) << 4) | ((lane & 3) << 2)));
-      const float v0 = bf16lo(w), v1 = bf16hi(w);
-#pragma unroll
-      for (int qi = 0; qi < NQ; ++qi) {
-        const float pj = __shfl_sync(0xffffffffu, pr[qi], j);
-        o0[qi] = fmaf(pj, v0, o0[qi]);
-        o1[qi] = fmaf(pj, v1, o1[qi]);
+      const float lw = warp_sum(l[qi]);
+      sm.red[warp][qi][2 * lane] = o0[qi];
+      sm.red[warp][qi][2 * lane + 1] = o1[qi];
+      if (lane == 0) {
+        sm.red[warp][qi][DK] = m[qi];
+        sm.red[warp][qi][DK + 1] = lw;
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&sm.empty[slot]));
-    // refill this slot with tile t + DSTAGES once every warp is done with it
-    if (producer && t + DSTAGES < ntiles) {
-      if (mbar_wait(smem_u32(&sm.empty[slot]), ph, p.limit_ns, abort)) {
-        mbar_arrive_expect_tx(smem_u32(&sm.full[slot]), 2 * TILE_BYTES);
-        tma_load_3d(smem_u32(sm.k[slot]), &tmk, smem_u32(&sm.full[slot]), 0,
-                    begin + (t + DSTAGES) * KT, bh);
-        tma_load_3d(smem_u32(sm.v[slot]), &tmv, smem_u32(&sm.full[slot]), 0,
-                    begin + (t + DSTAGES) * KT, bh);
+    __syncthreads();
+    // warp qi % NWARPS writes query qi
+    for (int qi = warp; qi < NQ; qi += NWARPS) {
+      float mm = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NWARPS; ++w) mm = fmaxf(mm, sm.red[w][qi][DK]);
+      const float base = mm == -INFINITY ? 0.f : mm;
+      float ll = 0.f, a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < NWARPS; ++w) {
+        const float f = ex2(sm.red[w][qi][DK] - base);
+        ll += f * sm.red[w][qi][DK + 1];
+        a0 += f * sm.red[w][qi][2 * lane];
+        a1 += f * sm.red[w][qi][2 * lane + 1];
+      }
+      const size_t row = static_cast<size_t>(bh) * NQ + qi;
+      if (p.splits == 1) {
+        const float inv = ll > 0.f ? 1.f / ll : 0.f;
+        reinterpret_cast<uint32_t*>(p.o + row * DK)[lane] = pack_bf16x2(a0 * inv, a1 * inv);
+        if (lane == 0 && p.lse != nullptr)
+          p.lse[row] = ll > 0.f ? (mm + __log2f(ll)) * LN2 : -INFINITY;
       } else {
-        atomicCAS(p.status, kDevOk, kDevTimeout);
-        *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+        float* dst =
+            p.part + ((static_cast<size_t>(bh) * p.splits + (u % p.splits)) * NQ + qi) * (DK + 2);
+        dst[2 * lane] = a0;
+        dst[2 * lane + 1] = a1;
+        if (lane == 0) {
+          dst[DK] = mm;
+          dst[DK + 1] = ll;
+        }
       }
     }
   }
-  if (!ok && lane == 0) {
-    atomicCAS(p.status, kDevOk, kDevTimeout);
+  if (!ok || !pok) {
+    if (lane == 0) atomicCAS(p.status, kDevOk, kDevTimeout);
     *reinterpret_cast<volatile int*>(&sm.abort) = 1;
   }
-  // Copies still in flight land before shared memory goes away.
+  // Copies still in flight land before shared memory goes away: the last
+  // tile issued to each slot.
   if (producer) {
     const int never = 0;
-    for (int i = 0; i < DSTAGES && i < ntiles; ++i) {
-      const int last = i + ((ntiles - 1 - i) / DSTAGES) * DSTAGES;  // last tile issued to slot i
+    for (uint32_t i = 0; i < DSTAGES && i < issued; ++i) {
+      const uint32_t last = i + ((issued - 1 - i) / DSTAGES) * DSTAGES;
       mbar_wait(smem_u32(&sm.full[i]), (last / DSTAGES) & 1, p.limit_ns, &never);
-    }
-  }
-
-  // ---- merge the four warps' states: lane sums, then across warps in smem
-#pragma unroll
-  for (int qi = 0; qi < NQ; ++qi) {
-    const float lw = warp_sum(l[qi]);
-    sm.red[warp][qi][2 * lane] = o0[qi];
-    sm.red[warp][qi][2 * lane + 1] = o1[qi];
-    if (lane == 0) {
-      sm.red[warp][qi][DK] = m[qi];
-      sm.red[warp][qi][DK + 1] = lw;
-    }
-  }
-  __syncthreads();
-  // warp qi % NWARPS writes query qi
-  for (int qi = warp; qi < NQ; qi += NWARPS) {
-    float mm = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NWARPS; ++w) mm = fmaxf(mm, sm.red[w][qi][DK]);
-    const float base = mm == -INFINITY ? 0.f : mm;
-    float ll = 0.f, a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int w = 0; w < NWARPS; ++w) {
-      const float f = ex2(sm.red[w][qi][DK] - base);
-      ll += f * sm.red[w][qi][DK + 1];
-      a0 += f * sm.red[w][qi][2 * lane];
-      a1 += f * sm.red[w][qi][2 * lane + 1];
-    }
-    const size_t row = static_cast<size_t>(bh) * NQ + qi;
-    if (p.splits == 1) {
-      const float inv = ll > 0.f ? 1.f / ll : 0.f;
-      reinterpret_cast<uint32_t*>(p.o + row * DK)[lane] = pack_bf16x2(a0 * inv, a1 * inv);
-      if (lane == 0 && p.lse != nullptr)
-        p.lse[row] = ll > 0.f ? (mm + __log2f(ll)) * LN2 : -INFINITY;
-    } else {
-      float* dst = p.part + ((static_cast<size_t>(bh) * p.splits + split) * NQ + qi) * (DK + 2);
-      dst[2 * lane] = a0;
-      dst[2 * lane + 1] = a1;
-      if (lane == 0) {
-        dst[DK] = mm;
-        dst[DK + 1] = ll;
-      }
     }
   }
 }
@@ -276,14 +362,17 @@ __global__ void __launch_bounds__(128)
 }
 
 template <int NQ>
-cudaError_t launch_split(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecParams& p,
-                         int BH, cudaStream_t stream) {
+cudaError_t launch_split(const CUtensorMap* maps, const DecParams& p, int BH, int num_sms,
+                         cudaStream_t stream) {
   const size_t smem = sizeof(DecSmem) + 1024;
   cudaError_t err = cudaFuncSetAttribute(attn_decode_split_kernel<NQ>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  attn_decode_split_kernel<NQ><<<dim3(p.splits, BH), THREADS, smem, stream>>>(tmk, tmv, p);
+  const int units = p.splits * BH;
+  const int grid = units < 3 * num_sms ? units : 3 * num_sms;  // three resident CTAs per SM
+  attn_decode_split_kernel<NQ><<<grid, THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3],
+                                                                  p);
   return cudaGetLastError();
 }
 
@@ -293,8 +382,9 @@ DecodePlan decode_plan(int B, int H, int n_q, int L_max, int num_sms) {
   DecodePlan plan;
   const long long bh = static_cast<long long>(B) * H;
   const int max_tiles = (L_max + KT - 1) / KT;
-  // about four CTAs per SM (two resident), and at least two tiles per chunk
-  const long long want = 4LL * num_sms;
+  // about four units per persistent CTA (three resident per SM), so that
+  // unequal cache lengths even out, and at least two tiles per chunk
+  const long long want = 4LL * 3 * num_sms;
   int splits = bh >= want ? 1 : static_cast<int>((want + bh - 1) / bh);
   splits = max(1, min(splits, max(1, max_tiles / 2)));
   const int tiles_per = (max_tiles + splits - 1) / splits;
@@ -306,8 +396,8 @@ DecodePlan decode_plan(int B, int H, int n_q, int L_max, int num_sms) {
   return plan;
 }
 
-cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                          const DecodePlan& plan, float* workspace, const LaunchCtx& ctx) {
+cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap* maps, const DecodePlan& plan,
+                          float* workspace, const LaunchCtx& ctx) {
   DecParams p;
   p.q = static_cast<const __nv_bfloat16*>(pb.q);
   p.cache_lens = pb.cache_lens;
@@ -315,6 +405,7 @@ cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap& tmk, const
   p.lse = pb.lse;
   p.part = workspace;
   p.H = pb.H;
+  p.BH = pb.B * pb.H;
   p.n_q = pb.n_q;
   p.L_max = pb.L_max;
   p.splits = plan.splits;
@@ -325,14 +416,14 @@ cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap& tmk, const
   const int BH = pb.B * pb.H;
   cudaError_t err;
   switch (pb.n_q) {
-    case 1: err = launch_split<1>(tmk, tmv, p, BH, ctx.stream); break;
-    case 2: err = launch_split<2>(tmk, tmv, p, BH, ctx.stream); break;
-    case 3: err = launch_split<3>(tmk, tmv, p, BH, ctx.stream); break;
-    case 4: err = launch_split<4>(tmk, tmv, p, BH, ctx.stream); break;
-    case 5: err = launch_split<5>(tmk, tmv, p, BH, ctx.stream); break;
-    case 6: err = launch_split<6>(tmk, tmv, p, BH, ctx.stream); break;
-    case 7: err = launch_split<7>(tmk, tmv, p, BH, ctx.stream); break;
-    case 8: err = launch_split<8>(tmk, tmv, p, BH, ctx.stream); break;
+    case 1: err = launch_split<1>(maps, p, BH, ctx.num_sms, ctx.stream); break;
+    case 2: err = launch_split<2>(maps, p, BH, ctx.num_sms, ctx.stream); break;
+    case 3: err = launch_split<3>(maps, p, BH, ctx.num_sms, ctx.stream); break;
+    case 4: err = launch_split<4>(maps, p, BH, ctx.num_sms, ctx.stream); break;
+    case 5: err = launch_split<5>(maps, p, BH, ctx.num_sms, ctx.stream); break;
+    case 6: err = launch_split<6>(maps, p, BH, ctx.num_sms, ctx.stream); break;
+    case 7: err = launch_split<7>(maps, p, BH, ctx.num_sms, ctx.stream); break;
+    case 8: err = launch_split<8>(maps, p, BH, ctx.num_sms, ctx.stream); break;
     default: return cudaErrorInvalidValue;
   }
   if (err != cudaSuccess || plan.splits == 1) return err;

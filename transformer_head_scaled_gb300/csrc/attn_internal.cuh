@@ -65,10 +65,11 @@ struct DecodePlan {
   size_t workspace_bytes;
 };
 DecodePlan decode_plan(int B, int H, int n_q, int L_max, int num_sms);
-// tmk / tmv describe the caches as 3-D (64, L_max, B*H) bf16 with a
-// (64, 128, 1) box and 128-byte swizzle; workspace holds plan.workspace_bytes.
-cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap& tmk, const CUtensorMap& tmv,
-                          const DecodePlan& plan, float* workspace, const LaunchCtx& ctx);
+// maps[0..3]: K cache, V cache as 3-D (64, L_max, B*H) bf16 with a
+// (64, 128, 1) box, then the same with a (64, 32, 1) box for partial last
+// tiles; all with 128-byte swizzle.  workspace holds plan.workspace_bytes.
+cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap* maps, const DecodePlan& plan,
+                          float* workspace, const LaunchCtx& ctx);
 
 // Diagnostics.  The tensor maps are 2-D (64, 128) bf16, one box each.
 cudaError_t launch_diag_tile(const CUtensorMap& tmq, const CUtensorMap& tmk,
