@@ -10,7 +10,9 @@ ctypes.  It computes eq. (1) of "Attention Is All You Need" (section 3.2.1),
 ``softmax(Q K^T / sqrt(d_k) + M) V``, with M = -inf on forbidden connections
 (section 3.2.3), plus the log-sum-exp of each row's scaled scores.  See the
 header of ``attn_oracle.c`` for the definition written out, and
-``tests/test_oracle.py`` for the pins that tie it to the pages.
+``tests/test_oracle.py`` for the pins that tie it to the pages.  The
+backward (``attn_bwd``) is the gradient of that forward, pinned in
+``tests/test_oracle_bwd.py`` by finite differences of the pinned forward.
 """
 from __future__ import annotations
 
@@ -65,6 +67,10 @@ def _load():
             g.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_long] * 6 + [
                 ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                 ctypes.c_long, ctypes.c_int]
+            h = lib.oracle_attn_bwd_f64
+            h.restype = ctypes.c_int
+            h.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_long] * 6 + [
+                ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -141,3 +147,22 @@ def attn_rows(q, k, v, rows, scale: float, mask_kind: int = MASK_NONE,
     if rc != 0:
         raise RuntimeError(f"oracle_attn_rows_f64 failed ({rc})")
     return o, lse
+
+
+def attn_bwd(q, k, v, dout, scale: float, mask_kind: int = MASK_NONE, key_lens=None,
+             threads: int = 0):
+    """Gradients (dq, dk, dv), float64, of a loss whose gradient with
+    respect to the forward's output O is ``dout`` [B,H,n_q,d_v]."""
+    q, k, v, kl, (B, H, n_q, n_k, d_k, d_v) = _prep(q, k, v, mask_kind, key_lens)
+    g = _as_f32(dout)
+    if g.shape != (B, H, n_q, d_v):
+        raise ValueError("dout must be [B,H,n_q,d_v]")
+    dq = np.empty((B, H, n_q, d_k), dtype=np.float64)
+    dk = np.empty((B, H, n_k, d_k), dtype=np.float64)
+    dv = np.empty((B, H, n_k, d_v), dtype=np.float64)
+    rc = _load().oracle_attn_bwd_f64(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(dq), _ptr(dk), _ptr(dv), B, H, n_q, n_k,
+        d_k, d_v, float(scale), int(mask_kind), _ptr(kl), int(threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_bwd_f64 failed ({rc})")
+    return dq, dk, dv

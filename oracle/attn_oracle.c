@@ -193,3 +193,115 @@ int oracle_max_threads(void) {
   return 1;
 #endif
 }
+
+/*
+ * Backward of the same operation: the gradients of a scalar loss through
+ * O = softmax(scale * Q K^T + M) V, given dO = dLoss/dO.  For each (b, h),
+ * with P the row-softmax matrix recomputed here from q, k (float64):
+ *
+ *   dV = P^T dO
+ *   dP = dO V^T
+ *   D_i = sum_c dO[i,c] * O[i,c]      (= sum_j P[i,j] dP[i,j])
+ *   dS = P (elementwise) (dP - D_i)   (the softmax Jacobian, row by row)
+ *   dQ = scale * dS K,   dK = scale * dS^T Q
+ *
+ * Forbidden connections have P = 0, hence dS = 0 there; a row with no
+ * visible key contributes nothing.  Inputs float32, arithmetic float64;
+ * layout as the forward, dO [B,H,n_q,d_v], dq/dk/dv like q/k/v.
+ * Returns 0, -1 on bad arguments, -2 when scratch cannot be allocated.
+ */
+int oracle_attn_bwd_f64(const float* q, const float* k, const float* v, const float* dout,
+                        double* dq, double* dk, double* dv, long B, long H, long n_q,
+                        long n_k, long d_k, long d_v, double scale, int mask_kind,
+                        const int* key_lens, int n_threads) {
+  if (oracle_check(B, H, n_q, n_k, d_k, d_v, mask_kind, key_lens)) return -1;
+  int failed = 0;
+#ifdef _OPENMP
+  if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (long bh = 0; bh < B * H; ++bh) {
+    const long b = bh / H;
+    const float* qb = q + bh * n_q * d_k;
+    const float* kb = k + bh * n_k * d_k;
+    const float* vb = v + bh * n_k * d_v;
+    const float* gb = dout + bh * n_q * d_v;
+    double* dqb = dq + bh * n_q * d_k;
+    double* dkb = dk + bh * n_k * d_k;
+    double* dvb = dv + bh * n_k * d_v;
+    double* P = (double*)malloc(sizeof(double) * (size_t)(n_q * n_k > 0 ? n_q * n_k : 1));
+    double* dS = (double*)malloc(sizeof(double) * (size_t)(n_q * n_k > 0 ? n_q * n_k : 1));
+    if (P == NULL || dS == NULL) {
+      free(P);
+      free(dS);
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+      failed = 1;
+      continue;
+    }
+    long limit = n_k;
+    if (mask_kind == ORACLE_MASK_KEY_PADDING) {
+      limit = key_lens[b];
+      if (limit > n_k) limit = n_k;
+      if (limit < 0) limit = 0;
+    }
+    /* P: the row softmax of the masked, scaled scores */
+    for (long i = 0; i < n_q; ++i) {
+      double m = -INFINITY;
+      for (long j = 0; j < n_k; ++j) {
+        int forbidden = (j >= limit) || (mask_kind == ORACLE_MASK_CAUSAL && j > i);
+        double s = -INFINITY;
+        if (!forbidden) {
+          double dot = 0.0;
+          for (long t = 0; t < d_k; ++t) dot += (double)qb[i * d_k + t] * (double)kb[j * d_k + t];
+          s = scale * dot;
+        }
+        P[i * n_k + j] = s;
+        if (s > m) m = s;
+      }
+      double Z = 0.0;
+      for (long j = 0; j < n_k; ++j) {
+        double w = (m == -INFINITY || P[i * n_k + j] == -INFINITY) ? 0.0 : exp(P[i * n_k + j] - m);
+        P[i * n_k + j] = w;
+        Z += w;
+      }
+      for (long j = 0; j < n_k; ++j) P[i * n_k + j] = Z > 0.0 ? P[i * n_k + j] / Z : 0.0;
+    }
+    /* dV = P^T dO */
+    for (long j = 0; j < n_k; ++j)
+      for (long c = 0; c < d_v; ++c) {
+        double acc = 0.0;
+        for (long i = 0; i < n_q; ++i) acc += P[i * n_k + j] * (double)gb[i * d_v + c];
+        dvb[j * d_v + c] = acc;
+      }
+    /* dS = P * (dP - D), dP = dO V^T, D_i = sum_j P_ij dP_ij */
+    for (long i = 0; i < n_q; ++i) {
+      double D = 0.0;
+      for (long j = 0; j < n_k; ++j) {
+        double dp = 0.0;
+        for (long c = 0; c < d_v; ++c) dp += (double)gb[i * d_v + c] * (double)vb[j * d_v + c];
+        dS[i * n_k + j] = dp;
+        D += P[i * n_k + j] * dp;
+      }
+      for (long j = 0; j < n_k; ++j) dS[i * n_k + j] = P[i * n_k + j] * (dS[i * n_k + j] - D);
+    }
+    /* dQ = scale dS K ; dK = scale dS^T Q */
+    for (long i = 0; i < n_q; ++i)
+      for (long t = 0; t < d_k; ++t) {
+        double acc = 0.0;
+        for (long j = 0; j < n_k; ++j) acc += dS[i * n_k + j] * (double)kb[j * d_k + t];
+        dqb[i * d_k + t] = scale * acc;
+      }
+    for (long j = 0; j < n_k; ++j)
+      for (long t = 0; t < d_k; ++t) {
+        double acc = 0.0;
+        for (long i = 0; i < n_q; ++i) acc += dS[i * n_k + j] * (double)qb[i * d_k + t];
+        dkb[j * d_k + t] = scale * acc;
+      }
+    free(P);
+    free(dS);
+  }
+  (void)n_threads;
+  return failed ? -2 : 0;
+}
