@@ -24,8 +24,9 @@
  * d_v = d_k, LSE [B,h,n_q] float32.
  *
  * Ownership and execution: every pointer argument is a device pointer owned
- * by the caller; the library reads q, k, v, key_lens and writes o and lse
- * only, never frees caller memory, and allocates no device memory.  Calls
+ * by the caller; the library reads its inputs and writes only the outputs
+ * (and workspace) each call names, never frees caller memory, and allocates
+ * no device memory.  Calls
  * are asynchronous on `stream` (NULL = the legacy default stream): argument
  * checks happen on the host before anything is enqueued; errors found on the
  * device are reported by attn_check().  No call synchronises the host.
@@ -140,6 +141,38 @@ size_t attn_decode_workspace_bytes(int B, int h, int n_q, int L_max, int d_k);
 int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o,
                         float* lse, int B, int h, int n_q, int L_max, int d_k, float scale,
                         const int* cache_lens, struct CUstream_st* stream);
+
+/*
+ * attn_bwd -- gradients of attn_fwd: given dout = dLoss/dO, writes
+ *   dq = dLoss/dQ, dk = dLoss/dK, dv = dLoss/dV
+ * for the same (q, k, v, scale, mask_kind, key_lens).  Per (b, h), with
+ * P = softmax(scale * Q K^T + M) recomputed from q, k and lse:
+ *   dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO[i,c] O[i,c],
+ *   dS = P * (dP - D_i),  dQ = scale dS K,  dK = scale dS^T Q.
+ * This is the back-propagation through eq. (1) of "Attention Is All You
+ * Need" (section 3.2.1) that training the model (section 5) needs; the
+ * paper does not write it out.
+ *   q, k, v  : bf16, as for attn_fwd (d_k must be 64, else ATTN_ERR_UNSUPPORTED).
+ *   o, lse   : the output and log-sum-exp attn_fwd returned for these inputs
+ *              (lse is required here).
+ *   dout     : bf16 [B, h, n_q, d_k].
+ *   dq, dk, dv : bf16 outputs shaped like q, k, v (rounded to nearest even).
+ *              Key rows past key_lens[b] (or that no query sees) get zeros.
+ *   workspace, workspace_bytes : caller-owned device scratch of at least
+ *              attn_bwd_workspace_bytes(B, h, n_q, d_k) bytes, 16-byte aligned
+ *              (per-row softmax statistics and an fp32 dQ accumulator); its
+ *              contents on entry do not matter.
+ * Products run on the tensor cores from bf16 operands with fp32
+ * accumulation; P and dS are rounded to bf16 before the products that use
+ * them.  Three kernels are enqueued on `stream`.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int B, int h, int n_q, int n_k,
+             int d_k, float scale, int mask_kind, const int* key_lens, void* workspace,
+             size_t workspace_bytes, struct CUstream_st* stream);
+
+/* Scratch bytes attn_bwd needs for these sizes (0 for unsupported sizes). */
+size_t attn_bwd_workspace_bytes(int B, int h, int n_q, int d_k);
 
 /*
  * attn_check -- synchronise `stream`, then report (and clear) any error a

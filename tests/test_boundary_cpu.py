@@ -126,3 +126,31 @@ def test_missing_library_fails_loudly(tmp_path):
             binding.load(str(tmp_path / "nope.so"))
     finally:
         binding._lib = saved
+
+
+def test_bwd_arguments_rejected_on_host(lib):
+    def call(q=A, k=A, v=A, o=A, dout=A, lse=A, dq=A, dk=A, dv=A, B=1, h=1, n_q=8, n_k=8, d=64,
+             scale=0.125, mask=0, lens=None, ws=A, ws_bytes=1 << 30):
+        return binding.attn_bwd_raw(q, k, v, o, dout, lse, dq, dk, dv, B, h, n_q, n_k, d, scale,
+                                    mask, lens, ws, ws_bytes, None)
+    INV, UNS = binding.ATTN_ERR_INVALID_ARG, binding.ATTN_ERR_UNSUPPORTED
+    for name in ("q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv", "ws"):
+        assert call(**{name: None}) == INV, name
+    for name in ("q", "k", "v", "o", "dout", "dq", "dk", "dv", "ws"):
+        assert call(**{name: A + 8}) == INV, name
+    assert call(lse=A + 2) == INV
+    assert call(n_q=0) == INV and call(n_k=0) == INV and call(B=0) == INV and call(h=-1) == INV
+    assert call(scale=0.0) == INV and call(scale=float("nan")) == INV
+    assert call(mask=2) == INV and call(mask=5) == INV
+    assert call(d=32) == UNS
+    need = lib.attn_bwd_workspace_bytes(2, 3, 200, 64)
+    assert call(B=2, h=3, n_q=200, ws_bytes=need - 1) == INV
+
+
+def test_bwd_workspace_size():
+    binding.load()
+    # per head: 2 x 256 padded rows of float32 statistics, then n_q x 64 float32
+    assert binding.bwd_workspace_bytes(2, 3, 200) == 6 * (2 * 256 * 4 + 200 * 64 * 4)
+    assert binding.bwd_workspace_bytes(1, 1, 128) == 2 * 128 * 4 + 128 * 64 * 4
+    assert binding.bwd_workspace_bytes(1, 1, 8, 32) == 0
+    assert binding.bwd_workspace_bytes(0, 1, 8) == 0

@@ -29,7 +29,7 @@ DECODE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 # Every entry point declared in include/attn.h.
 EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_decode", "attn_decode_workspace_bytes",
-           "attn_decode_noalloc",
+           "attn_decode_noalloc", "attn_bwd", "attn_bwd_workspace_bytes",
            "attn_check", "attn_status_string",
            "attn_last_cuda_error", "attn_set_wait_limit_ns", "attn_launch_count",
            "attn_diag_tile", "attn_diag_wait_timeout")
@@ -71,6 +71,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                             vp]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+        lib.attn_bwd.restype = i32
+        lib.attn_bwd.argtypes = [vp] * 9 + [i32] * 5 + [f32, i32, vp, vp, ctypes.c_size_t, vp]
+        lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32]
         lib.attn_check.restype = i32
         lib.attn_check.argtypes = [vp]
         lib.attn_status_string.restype = ctypes.c_char_p
@@ -208,6 +212,66 @@ def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode")
     return out, lse
+
+
+def bwd_workspace_bytes(B: int, h: int, n_q: int, d: int = 64) -> int:
+    """Scratch bytes attn_bwd needs (0 for unsupported sizes)."""
+    return int(load().attn_bwd_workspace_bytes(B, h, n_q, d))
+
+
+def attn_bwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, dout_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr, B, h,
+                 n_q, n_k, d, scale, mask_kind, lens_ptr, ws_ptr, ws_bytes, stream_ptr) -> int:
+    """The C call itself, on raw device pointers; returns the status code."""
+    return load().attn_bwd(q_ptr, k_ptr, v_ptr, o_ptr, dout_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr,
+                           B, h, n_q, n_k, d, float(scale), int(mask_kind), lens_ptr, ws_ptr,
+                           int(ws_bytes), stream_ptr)
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+             lse: torch.Tensor, dout: torch.Tensor, scale: float | None = None,
+             mask: int = MASK_NONE, key_lens: torch.Tensor | None = None,
+             dq: torch.Tensor | None = None, dk: torch.Tensor | None = None,
+             dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """Gradients (dq, dk, dv) of attn_fwd for dout = dLoss/dO.
+
+    q, k, v, o, dout: contiguous bf16 CUDA [B, h, n, 64] tensors; o and lse
+    are what attn_fwd returned for q, k, v with the same scale and mask.
+    A workspace of bwd_workspace_bytes(...) is allocated when none is given.
+    """
+    for t in (q, k, v, o, dout):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError("q, k, v, o, dout must be contiguous bf16 CUDA [B, h, n, d] tensors")
+    B, h, n_q, d = q.shape
+    n_k = k.shape[2]
+    if tuple(k.shape) != (B, h, n_k, d) or tuple(v.shape) != (B, h, n_k, d):
+        raise ValueError("k and v must be [B, h, n_k, d] with q's B, h, d")
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("o and dout must be shaped like q")
+    if (lse is None or not lse.is_cuda or lse.dtype != torch.float32
+            or tuple(lse.shape) != (B, h, n_q) or not lse.is_contiguous()):
+        raise ValueError("lse must be the forward's contiguous float32 [B, h, n_q] CUDA tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    kl = None
+    if mask == MASK_KEY_PADDING:
+        if key_lens is None:
+            raise ValueError("key padding needs key_lens")
+        kl = key_lens
+        if kl.dtype != torch.int32 or not kl.is_cuda or kl.numel() != B or not kl.is_contiguous():
+            raise ValueError("key_lens must be a contiguous int32 CUDA tensor of B entries")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = bwd_workspace_bytes(B, h, n_q, d)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = attn_bwd_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                      _ptr(dk), _ptr(dv), B, h, n_q, n_k, d, scale, int(mask), _ptr(kl),
+                      _ptr(workspace), ws_bytes, _stream_ptr(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def check(stream=None) -> None:

@@ -121,6 +121,20 @@ int encode_3d(CUtensorMap* map, const void* base, int d, int n, long long bh, in
   return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
 }
 
+// (64, n, B*H) fp32 view with a (32, 128, 1) box and 128-byte swizzle (the
+// backward's dQ accumulator, added into by TMA reduce).
+int encode_3d_f32(CUtensorMap* map, const void* base, int n, long long bh) {
+  cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {256u, 256u * static_cast<cuuint64_t>(n)};
+  cuuint32_t box[3] = {32u, 128u, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
+}
+
 int encode_2d(CUtensorMap* map, const void* base) {
   cuuint64_t dims[2] = {64, 128};
   cuuint64_t strides[1] = {128};
@@ -279,6 +293,46 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                 make_ctx(*di, stream));
   if (e != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(plan.splits > 1 ? 2 : 1);
+  return ATTN_OK;
+}
+
+size_t attn_bwd_workspace_bytes(int B, int h, int n_q, int d_k) {
+  if (B < 1 || h < 1 || n_q < 1 || d_k != 64) return 0;
+  if (static_cast<long long>(B) * h > 0x7fffffffLL) return 0;
+  return bwd_layout(B, h, n_q).bytes;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int B, int h, int n_q, int n_k,
+             int d_k, float scale, int mask_kind, const int* key_lens, void* workspace,
+             size_t workspace_bytes, struct CUstream_st* stream) {
+  int rc = check_common(q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, mask_kind, key_lens, 2);
+  if (rc != ATTN_OK) return rc;
+  if (!dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(workspace))
+    return ATTN_ERR_INVALID_ARG;
+  if (d_k != 64) return ATTN_ERR_UNSUPPORTED;
+  const BwdLayout lay = bwd_layout(B, h, n_q);
+  if (workspace_bytes < lay.bytes) return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di)) != ATTN_OK) return rc;
+  const long long bh = static_cast<long long>(B) * h;
+  CUtensorMap maps[7];
+  if ((rc = encode_3d(&maps[0], q, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&maps[1], k, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&maps[2], v, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&maps[3], dout, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&maps[4], dk, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&maps[5], dv, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d_f32(&maps[6], static_cast<uint8_t*>(workspace) + lay.dq_acc_off, n_q, bh)) !=
+      ATTN_OK)
+    return rc;
+  BwdProblem pb{q, k, v, o, dout, lse, dq, dk, dv, B, h, n_q, n_k, scale, mask_kind,
+                mask_kind == ATTN_MASK_KEY_PADDING ? key_lens : nullptr};
+  cudaError_t e = launch_bwd(pb, maps, workspace, make_ctx(*di, stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(3);
   return ATTN_OK;
 }
 

@@ -71,6 +71,36 @@ DecodePlan decode_plan(int B, int H, int n_q, int L_max, int num_sms);
 cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap* maps, const DecodePlan& plan,
                           float* workspace, const LaunchCtx& ctx);
 
+// Backward (d = 64, bf16): gradients of the forward above.
+struct BwdProblem {
+  const void* q;     // bf16 [B, H, n_q, 64]
+  const void* k;     // bf16 [B, H, n_k, 64]
+  const void* v;
+  const void* o;     // the forward's output, bf16 [B, H, n_q, 64]
+  const void* dout;  // dLoss/dO, bf16 [B, H, n_q, 64]
+  const float* lse;  // the forward's log-sum-exp [B, H, n_q]
+  void* dq;          // bf16 outputs, shaped like q, k, v
+  void* dk;
+  void* dv;
+  int B, H, n_q, n_k;
+  float scale;
+  int mask;
+  const int* key_lens;
+};
+
+// Workspace of the backward: -LSE*log2(e) and -D per query row (rows padded
+// to a multiple of 128 per head), then the fp32 dQ accumulator [B, H, n_q, 64].
+struct BwdLayout {
+  size_t nq_pad, nlse2_off, nd_off, dq_acc_off, bytes;
+};
+BwdLayout bwd_layout(int B, int H, int n_q);
+size_t bwd_tc_smem_bytes();
+// maps: Q, K, V, dO, dK, dV as 3-D (64, n, B*H) bf16 with a (64, 128, 1) box,
+// then the dQ accumulator as 3-D (64, n_q, B*H) fp32 with a (32, 128, 1) box;
+// all with 128-byte swizzle.  Three launches (preprocess, main, dQ convert).
+cudaError_t launch_bwd(const BwdProblem& pb, const CUtensorMap* maps, void* workspace,
+                       const LaunchCtx& ctx);
+
 // Diagnostics.  The tensor maps are 2-D (64, 128) bf16, one box each.
 cudaError_t launch_diag_tile(const CUtensorMap& tmq, const CUtensorMap& tmk,
                              const CUtensorMap& tmv, const void* p, float* s, float* o,
