@@ -7,6 +7,12 @@ mask, online softmax, PV, epilogue) over one batch of the workload.  The
 default workload is the base encoder self-attention (B=64, h=8, n_q=n_k=512,
 d_k=d_v=64, bf16, no mask).  Prints ONE JSON line (rank 0).
 
+Backward workloads (names ending in ``_bwd``): one step = one ``attn_bwd``
+call (its three kernels) on the same problems, O and LSE computed once by the
+forward beforehand; FLOPs count the five n_q x n_k x d products of the
+backward (2.5 times the forward's).  Decoding workloads: one ``attn_decode``
+call, reported against HBM bandwidth.
+
 Timing: W untimed warm-up steps, then K timed steps.  Before every timed step
 the L2 is flushed by writing a 256 MiB buffer (outside the timed interval);
 each step is bracketed by CUDA events on the launching stream, and the whole
@@ -40,14 +46,32 @@ from transformer_head_scaled_gb300 import inputs, shard  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20
 METRIC = "fused attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor peak"
-KERNEL_SOURCES = ("transformer_head_scaled_gb300/csrc/attn_fwd_tc.cu",
-                  "transformer_head_scaled_gb300/csrc/ptx.cuh")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_tc_traffic.json")
+METRIC_BWD = "fused attention bwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor peak"
 
 
-def kernel_hash() -> str:
+def metric_name(w: inputs.Workload) -> str:
+    """The forward's metric; backward workloads report the same quantity for the backward."""
+    return METRIC_BWD if w.kind == "bwd" else METRIC
+
+
+# The sources of each pass's main kernel, and the committed ncu DRAM bytes per
+# launch measured for that exact source (matched by hash).
+_CSRC = "transformer_head_scaled_gb300/csrc/"
+KERNEL_SOURCES = {
+    "fwd": (_CSRC + "attn_fwd_tc.cu", _CSRC + "ptx.cuh"),
+    "bwd": (_CSRC + "attn_bwd.cu", _CSRC + "ptx.cuh"),
+    "decode": (_CSRC + "attn_decode.cu", _CSRC + "ptx.cuh"),
+}
+TRAFFIC_FILES = {
+    "fwd": os.path.join(ROOT, "profiles", "attn_fwd_tc_traffic.json"),
+    "bwd": os.path.join(ROOT, "profiles", "attn_bwd_tc_traffic.json"),
+    "decode": os.path.join(ROOT, "profiles", "attn_decode_traffic.json"),
+}
+
+
+def kernel_hash(kind: str = "fwd") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -64,14 +88,16 @@ def measured_peaks() -> dict:
             "_source": "fallback"}
 
 
-def dram_traffic(workload: str):
-    """ncu DRAM bytes per launch for this kernel source and workload, or None."""
-    if not os.path.exists(TRAFFIC_FILE):
+def dram_traffic(w: inputs.Workload):
+    """ncu DRAM bytes per launch of this pass's main kernel for its current
+    source and this workload, or None."""
+    path = TRAFFIC_FILES[w.kind]
+    if not os.path.exists(path):
         return None
-    with open(TRAFFIC_FILE) as f:
+    with open(path) as f:
         d = json.load(f)
-    e = d.get(workload)
-    if not e or e.get("kernel_hash") != kernel_hash():
+    e = d.get(w.name)
+    if not e or e.get("kernel_hash") != kernel_hash(w.kind):
         return None
     return e.get("bytes_per_launch")
 
@@ -190,6 +216,42 @@ def oracle_sample(w: inputs.Workload, q, k, v, kl, target_s: float, threads: int
     return flops / dt / 1e12, dt, done, flops
 
 
+def oracle_bwd_sample(w: inputs.Workload, q, k, v, g, kl, target_s: float, threads: int = 0,
+                      heads_hint: int | None = None):
+    """Time the float64 oracle's backward on whole sampled heads (a head's
+    gradients depend only on its own data), about target_s seconds of work.
+    Returns (tflops, seconds, heads_done, flops)."""
+    import oracle
+    oracle.build()
+    BH = w.B * w.h
+    lens = None if kl is None else np.asarray(kl.cpu()).astype(np.int32)
+    rng = np.random.default_rng(321)
+
+    def run(sel):
+        b_idx, h_idx = sel // w.h, sel % w.h
+        sub = lambda t: np.ascontiguousarray(t[b_idx, h_idx][:, None])  # noqa: E731
+        sl = None if lens is None else lens[b_idx]
+        t0 = time.perf_counter()
+        oracle.attn_bwd(sub(q), sub(k), sub(v), sub(g), w.scale, w.mask, sl, threads=threads)
+        dt = time.perf_counter() - t0
+        rows = np.concatenate([np.arange(w.n_q) + int(bh) * w.n_q for bh in sel])
+        return dt, _row_flops(w, rows, lens) * inputs.products(w) / 2.0
+
+    if heads_hint is None:
+        n = min(BH, max(1, oracle.max_threads()))
+        dt, _ = run(np.sort(rng.choice(BH, size=n, replace=False)))
+        heads_hint = max(1, int(n * target_s / max(dt, 1e-9)))
+    done, flops, dt = 0, 0.0, 0.0
+    while done < heads_hint:
+        n = min(BH, heads_hint - done)
+        sel = np.sort(rng.choice(BH, size=n, replace=False))
+        d, f = run(sel)
+        dt += d
+        flops += f
+        done += n
+    return flops / dt / 1e12, dt, done, flops
+
+
 def cpu_cores_used() -> int:
     import oracle
     return oracle.max_threads()
@@ -203,30 +265,41 @@ def run_reference(args, w):
         return 0
     q, k, v, kl = inputs.make_inputs(w)
     qf, kf, vf = q.float().numpy(), k.float().numpy(), v.float().numpy()
+    bwd = w.kind == "bwd"
+    gf = inputs.make_dout(w).float().numpy() if bwd else None
     # the whole run (warm-up included) is sized to about two minutes of CPU time
     per_step = min(20.0, 120.0 / max(1, args.steps + args.warmup))
-    _, dt, n, _ = oracle_sample(w, qf, kf, vf, kl, target_s=min(per_step, 1.0))
-    rows_per_step = max(1, int(n * per_step / max(dt, 1e-9)))
+    if bwd:
+        sample = lambda target, hint: oracle_bwd_sample(  # noqa: E731
+            w, qf, kf, vf, gf, kl, target, heads_hint=hint)
+    else:
+        sample = lambda target, hint: oracle_sample(  # noqa: E731
+            w, qf, kf, vf, kl, target, rows_hint=hint)
+    _, dt, n, _ = sample(min(per_step, 1.0), None)
+    per_step_units = max(1, int(n * per_step / max(dt, 1e-9)))
     for _ in range(args.warmup):
-        oracle_sample(w, qf, kf, vf, kl, 0.0, rows_hint=rows_per_step)
+        sample(0.0, per_step_units)
     vals, secs = [], []
     for _ in range(args.steps):
-        tf, dt, _, _ = oracle_sample(w, qf, kf, vf, kl, 0.0, rows_hint=rows_per_step)
+        tf, dt, _, _ = sample(0.0, per_step_units)
         vals.append(tf)
         secs.append(dt)
-    rows_used = rows_per_step
     value = statistics.median(vals)
     cores = cpu_cores_used()
-    sample = (f"{rows_used} query rows per step, drawn from the {w.B * w.h * w.n_q} rows of the "
-              f"workload (each against all its visible keys), float64")
+    if bwd:
+        desc = (f"{per_step_units} whole heads per step, drawn from the {w.B * w.h} heads of the "
+                f"workload (dQ, dK, dV of each), float64")
+    else:
+        desc = (f"{per_step_units} query rows per step, drawn from the {w.B * w.h * w.n_q} rows "
+                f"of the workload (each against all its visible keys), float64")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": metric_name(w), "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_desc(w), "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -259,18 +332,35 @@ def run_ours(args, w):
     ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
     klp = None if kl is None else kl.data_ptr()
     decode = w.kind == "decode"
-    ws_bytes = binding.decode_workspace_bytes(w.B, w.h, w.n_q, w.n_k, w.d) if decode else 0
+    bwd = w.kind == "bwd"
+    if decode:
+        ws_bytes = binding.decode_workspace_bytes(w.B, w.h, w.n_q, w.n_k, w.d)
+    elif bwd:
+        ws_bytes = binding.bwd_workspace_bytes(w.B, w.h, w.n_q, w.d)
+    else:
+        ws_bytes = 0
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    g = None
+    if bwd:
+        # O and LSE of the same inputs come from the forward, outside the timing
+        g = inputs.make_dout(w, device=dev, seed=inputs.SEED_DOUT + 8 * rank)
+        binding.attn_fwd(q, k, v, scale=w.scale, mask=w.mask, key_lens=kl, out=o, lse=lse)
+        grads = [torch.empty_like(t) for t in (q, k, v)]
+        bptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), g.data_ptr(),
+                 lse.data_ptr(), *(t.data_ptr() for t in grads))
 
     def step():
         if decode:
             rc = binding.attn_decode_raw(*ptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale, klp,
                                          ws.data_ptr(), ws_bytes, sptr)
+        elif bwd:
+            rc = binding.attn_bwd_raw(*bptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale, w.mask, klp,
+                                      ws.data_ptr(), ws_bytes, sptr)
         else:
             rc = binding.attn_fwd_raw(*ptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale, w.mask, klp,
                                       sptr, f32=f32)
         if rc != 0:
-            raise binding.AttnError(rc, "attn_decode" if decode else "attn_fwd")
+            raise binding.AttnError(rc, w.kind)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -309,12 +399,13 @@ def run_ours(args, w):
     achieved = fl_alg / (ms * 1e-3) / 1e12
     hbm = inputs.hbm_bytes(w, kl)
 
-    # end to end through the public API: pinned host inputs -> device -> attn_fwd -> host
-    e2e = run_e2e(args, w, q, k, v, kl, dev, stream, f32)
+    # end to end through the public API: pinned host inputs -> device -> call -> host
+    e2e = (run_e2e_bwd(args, w, q, k, v, o, lse, g, kl, dev, stream) if bwd else
+           run_e2e(args, w, q, k, v, kl, dev, stream, f32))
 
     clk = clocks.summary(t_start, t_end)
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "metric": metric_name(w), "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if f32 else "bf16", "data": "synthetic",
@@ -326,15 +417,17 @@ def run_ours(args, w):
         "pct_of_peak": 100.0 * (value / world) / peaks["bf16_tflops"],
         "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                       "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                      "traffic": dram_traffic(w.name),
+                      "traffic": dram_traffic(w),
                       "peak_source": f"{peaks['_source']} bf16_tflops (burst; kernel timed alone)",
                       "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                       "hbm_gbs": hbm / (ms * 1e-3) / 1e9,
-                      "kernel": "attn_fwd_tc_kernel" if not f32 else "attn_fwd_f32_kernel"}
+                      "kernel": ("attn_bwd_tc_kernel, timed together with its preprocess and "
+                                 "dQ-convert launches (one C call)") if bwd else
+                                ("attn_fwd_tc_kernel" if not f32 else "attn_fwd_f32_kernel")}
                      if not decode else
                      {"bound": "hbm", "achieved": hbm / (ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                       "unit": "GB/s", "frac": hbm / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                      "traffic": dram_traffic(w.name), "algorithmic_bytes": hbm,
+                      "traffic": dram_traffic(w), "algorithmic_bytes": hbm,
                       "peak_source": f"{peaks['_source']} hbm_gbs (copy bandwidth)",
                       "kernel": "attn_decode_split_kernel" + (" + combine" if ws_bytes else "")}),
         "e2e": e2e,
@@ -343,11 +436,17 @@ def run_ours(args, w):
     }
     if rank == 0 and not args.no_cpu_baseline:
         qf, kf, vf = (t.float().cpu().numpy() for t in (q, k, v))
-        tf, dt, nrows, _ = oracle_sample(w, qf, kf, vf, kl, target_s=args.cpu_seconds)
-        line["cpu_baseline"] = {
-            "value": tf, "unit": "TFLOP/s", "cores": cpu_cores_used(), "kind": "oracle",
-            "sample": f"{nrows} query rows ({nrows / (w.B * w.h * w.n_q):.2f} passes over the "
-                      f"{w.B * w.h * w.n_q} rows of the same workload), float64, {dt:.1f} s"}
+        if bwd:
+            gf = g.float().cpu().numpy()
+            tf, dt, nh, _ = oracle_bwd_sample(w, qf, kf, vf, gf, kl, target_s=args.cpu_seconds)
+            desc = (f"{nh} whole heads of the {w.B * w.h} of the same workload (dQ, dK, dV of "
+                    f"each), float64, {dt:.1f} s")
+        else:
+            tf, dt, nrows, _ = oracle_sample(w, qf, kf, vf, kl, target_s=args.cpu_seconds)
+            desc = (f"{nrows} query rows ({nrows / (w.B * w.h * w.n_q):.2f} passes over the "
+                    f"{w.B * w.h * w.n_q} rows of the same workload), float64, {dt:.1f} s")
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cpu_cores_used(),
+                                "kind": "oracle", "sample": desc}
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
@@ -393,6 +492,56 @@ def run_e2e(args, w, q, k, v, kl, dev, stream, f32):
             raise binding.AttnError(rc, "attention")
         ho.copy_(do, non_blocking=True)
         hl.copy_(dl, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    n = max(3, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    binding.check(stream)
+    ms = e0.elapsed_time(e1) / n
+    world = dist_env()[0]
+    return {"value": world * inputs.flops(w) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms,
+            "steps": n}
+
+
+def run_e2e_bwd(args, w, q, k, v, o, lse, g, kl, dev, stream):
+    """The backward end to end: Q, K, V, O, LSE, dO (and key lengths) copied in
+    from pinned host memory, dQ, dK, dV copied back, every step."""
+    from transformer_head_scaled_gb300 import binding
+    host_in = [t.cpu().pin_memory() for t in (q, k, v, o, lse, g)]
+    hkl = None if kl is None else kl.cpu().pin_memory()
+    dev_in = [torch.empty_like(t) for t in (q, k, v, o, lse, g)]
+    dkl = None if kl is None else torch.empty_like(kl)
+    dev_out = [torch.empty_like(t) for t in (q, k, v)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out]
+    ws_bytes = binding.bwd_workspace_bytes(w.B, w.h, w.n_q, w.d)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host_in) + (0 if hkl is None else hkl.numel() * 4)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    sptr = int(stream.cuda_stream)
+
+    def step():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        if dkl is not None:
+            dkl.copy_(hkl, non_blocking=True)
+        qd, kd, vd, od, ld, gd = dev_in
+        rc = binding.attn_bwd_raw(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(),
+                                  gd.data_ptr(), ld.data_ptr(),
+                                  *(t.data_ptr() for t in dev_out), w.B, w.h, w.n_q, w.n_k,
+                                  w.d, w.scale, w.mask, None if dkl is None else dkl.data_ptr(),
+                                  ws.data_ptr(), ws_bytes, sptr)
+        if rc != 0:
+            raise binding.AttnError(rc, "attn_bwd")
+        for h, d in zip(host_out, dev_out):
+            h.copy_(d, non_blocking=True)
 
     for _ in range(3):
         step()

@@ -149,8 +149,8 @@ def test_bwd_arguments_rejected_on_host(lib):
 
 def test_bwd_workspace_size():
     binding.load()
-    # per head: 2 x 256 padded rows of float32 statistics, then n_q x 64 float32
-    assert binding.bwd_workspace_bytes(2, 3, 200) == 6 * (2 * 256 * 4 + 200 * 64 * 4)
-    assert binding.bwd_workspace_bytes(1, 1, 128) == 2 * 128 * 4 + 128 * 64 * 4
+    # per head and 128-query tile a 4 KB constant tile, then n_q x 64 float32
+    assert binding.bwd_workspace_bytes(2, 3, 200) == 6 * (2 * 4096 + 200 * 64 * 4)
+    assert binding.bwd_workspace_bytes(1, 1, 128) == 4096 + 128 * 64 * 4
     assert binding.bwd_workspace_bytes(1, 1, 8, 32) == 0
     assert binding.bwd_workspace_bytes(0, 1, 8) == 0

@@ -11,35 +11,45 @@
 //   dS = P * (dP - D_i)  (elementwise),   dQ = scale dS K,   dK = scale dS^T Q.
 //
 // Three launches:
-//   1. attn_bwd_pre_kernel: per query row, -D_i and -LSE_i * log2(e) into the
-//      workspace (zero on the padding rows of each 128-row tile), and the row
-//      of the fp32 dQ accumulator set to zero.
+//   1. attn_bwd_pre_kernel: per query row, the two per-query constants the
+//      elementwise steps need, b_i = -LSE_i / scale and -D_i, each split into
+//      three bf16 parts (hi + mid + lo) and written as [128 x 16] bf16 tiles;
+//      and the row of the fp32 dQ accumulator set to zero.
 //   2. attn_bwd_tc_kernel: one persistent CTA per SM walks work items = one
 //      128-key tile of one (b, h); for each 128-query tile that the mask lets
-//      see those keys it runs the five tensor-core products of that tile pair
-//      and accumulates dK and dV in tensor memory; dQ of the tile pair is
-//      added into the fp32 accumulator in global memory with a TMA reduce.
+//      see those keys it runs the tensor-core products of that tile pair and
+//      accumulates dK and dV in tensor memory; dQ of the tile pair is added
+//      into the fp32 accumulator in global memory with a TMA reduce.
 //   3. attn_bwd_dq_kernel: dQ = scale * accumulator, rounded to bf16.
 //
+// The per-query constants ride on the tensor cores: one extra K=16 step
+// against an all-ones operand adds b_i to every score of column i and -D_i to
+// every dP of column i,
+//   S'^T = K Q^T + 1 b^T,   dP'^T = V dO^T + 1 (-D)^T,
+// so that the elementwise work per element is P = 2^(scale*log2(e) * S') and
+// dS = P * dP' (the three bf16 parts keep b and D to about 2^-24 relative).
+//
 // Kernel 2 (448 threads):
-//   warps 0-7   the elementwise part: warp w owns tensor-memory lanes
-//               32*(w%4).. (= keys) and query columns 64*(w/4)..+63; it turns
-//               S^T into P^T and dP^T into dS^T and writes both, as bf16, into
-//               shared memory in the 128-byte swizzled layout the MMAs read;
+//   warps 0-7   elementwise: warp w owns tensor-memory lanes 32*(w%4).. (=
+//               keys) and query columns 64*(w/4)..+63; it turns S'^T into P^T
+//               (bf16, written to tensor memory) and dP'^T into dS^T (bf16,
+//               written to shared memory in the 128-byte swizzled layout);
 //   warps 8-11  epilogue: dQ of each tile pair (tensor memory -> swizzled fp32
 //               staging -> TMA reduce-add), dK and dV of each item (-> bf16 ->
 //               TMA store);
-//   warp  12    TMA producer: K, V per item (2 slots), Q, dO, -LSE2, -D per
-//               query tile (2 stages);
+//   warp  12    TMA producer: K, V per item (2 slots); Q, dO and the two
+//               constant tiles per query tile (3 stages);
 //   warp  13    tensor-memory owner and MMA issuer.
-// Tensor memory (512 columns): S^T [0,128)  dP^T [128,256)  dV [256,320)
-// dK [320,384)  dQ [384,448).  Keys are the 128 lanes of S^T, dP^T, dV, dK;
-// queries are the lanes of dQ.
-// Per tile pair t the MMAs are issued in the order
-//   dV(t), S^T(t+1), dP^T(t+1), dK(t), dQ(t)
-// so that the elementwise warps can start on tile t+1 while the tensor pipe
-// finishes the gradient products of tile t.  Every wait is bounded; on timeout
-// the kernel records kDevTimeout, all roles drain and the CTA returns.
+// Tensor memory (512 columns): S'^T [0,128)  dP'^T [128,256)  dV [256,320)
+// dK [320,384)  dQ [384,448)  P^T [448,512) (bf16 pairs).  Keys are the 128
+// lanes of all but dQ, whose lanes are queries.
+// Products per tile pair t (all 128-row M; * = from tensor memory):
+//   S'^T = K Q^T (+1 b^T)    dP'^T = V dO^T (+1 (-D)^T)    dV += P^T* dO
+//   dK += dS^T Q             dQ = dS K
+// issued in the order S'(t+1), dV(t), dP'(t+1), dK(t), dQ(t), so that the
+// elementwise warps start on tile t+1 while the tensor pipe finishes the
+// gradient products of tile t.  Every wait is bounded; on timeout the kernel
+// records kDevTimeout, all roles drain and the CTA returns.
 #include <cuda_bf16.h>
 
 #include "attn_internal.cuh"
@@ -54,12 +64,23 @@ constexpr int BM = 128;  // queries per query tile
 constexpr int BN = 128;  // keys per key tile (= tensor-memory lanes)
 constexpr int D = 64;    // head size
 constexpr uint32_t TILE_BYTES = 128 * D * 2;  // a [128 x 64] bf16 tile: 16 KB
+// Q (and its constant tile) ring: Q is last read by dK, late in a tile pair,
+// so three stages let the next tile's loads start two tile pairs ahead.  dO
+// is last read by dV, early in a tile pair: two stages suffice.
+constexpr int QSTAGES = 3;
+constexpr int OSTAGES = 2;
 constexpr int NUM_THREADS = 448;
 constexpr int EPI_WARP0 = 8;
 constexpr int LOAD_WARP = 12;
 constexpr int MMA_WARP = 13;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 320, COL_DQ = 384;
+constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 320, COL_DQ = 384,
+                   COL_PT = 448;
+// The [128 x 16] bf16 constant tile of a query tile (K-major, no swizzle:
+// 8-row x 16-byte core matrices, the second 8 columns 128 B after the first,
+// 8-row groups 256 B apart).  Row i holds b_i in columns 0-2 (hi, mid, lo)
+// and -D_i in columns 3-5; columns 6-15 are zero.
+constexpr uint32_t CONST_TILE_BYTES = 128 * 16 * 2;
 constexpr int EPI_BAR = 1;  // named barrier of the 128 epilogue threads
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -68,17 +89,19 @@ static_assert(BM == BN, "the causal tile range assumes square tiles");
 struct __align__(1024) Smem {
   uint8_t k[2][TILE_BYTES];
   uint8_t v[2][TILE_BYTES];
-  uint8_t q[2][TILE_BYTES];
-  uint8_t dout[2][TILE_BYTES];
-  // P^T and dS^T as [128 keys x 128 queries] bf16: two 64-query column blocks
-  // of [128 x 64], each in the 128-byte swizzled layout.
-  uint8_t pt[2][TILE_BYTES];
+  uint8_t q[QSTAGES][TILE_BYTES];
+  uint8_t dout[OSTAGES][TILE_BYTES];
+  // dS^T as [128 keys x 128 queries] bf16: two 64-query column blocks of
+  // [128 x 64], each in the 128-byte swizzled layout.
   uint8_t dst[2][TILE_BYTES];
-  uint8_t stage[TILE_BYTES];  // epilogue staging (fp32 half of dQ, or bf16 dK / dV)
-  float nlse2[2][BM];         // -LSE * log2(e) of the stage's queries
-  float nd[2][BM];            // -D of the stage's queries
+  uint8_t stage[2][TILE_BYTES];  // epilogue staging (the two fp32 halves of dQ, or dV and dK)
+  uint8_t cst[QSTAGES][CONST_TILE_BYTES];  // the constant tile of each Q stage
+  // Two 8 x 8 bf16 core matrices that select columns of the constant tile:
+  // [0] rows (1,1,1,0,0,0,0,0) picks b, [1] rows (0,0,0,1,1,1,0,0) picks -D.
+  uint8_t sel[2][512];
   uint64_t kv_full[2], kv_empty[2];
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[QSTAGES], q_empty[QSTAGES];
+  uint64_t o_full[OSTAGES], o_empty[OSTAGES];
   uint64_t s_full, s_free, dp_full, dp_free;
   uint64_t p_full, p_free, ds_full, ds_free;
   uint64_t dq_full, dq_free, dkv_full, dkv_free;
@@ -88,10 +111,9 @@ struct __align__(1024) Smem {
 };
 
 struct Params {
-  const float* nlse2;  // [BH][nq_pad]
-  const float* nd;     // [BH][nq_pad]
+  const uint8_t* cst;  // constant tiles [BH][num_qt][2][CONST_TILE_BYTES]
   const int* key_lens;
-  int H, n_q, n_k, BH, nq_pad;
+  int H, n_q, n_k, BH;
   int mask;
   int num_qt, num_kt, num_items;
   float scale_log2;  // scale * log2(e)
@@ -171,12 +193,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr));
-  return v;
+// Shared-memory matrix descriptor without swizzle (K-major: 8-row x 16-byte
+// core matrices; LBO = byte step between the two 8-column halves of K = 16,
+// SBO = byte step between 8-row groups).  Same fields as the 128-byte swizzle
+// descriptor with layout bits 61-63 = 0.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t smem_addr, uint32_t lbo_bytes,
+                                                uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  return d;
 }
 
 // One row (128 bytes = eight 16-byte chunks) into a 128-byte swizzled tile:
@@ -209,8 +237,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sm.kv_full[i]), 1);
       mbar_init(smem_u32(&sm.kv_empty[i]), 1);
+    }
+    for (int i = 0; i < QSTAGES; ++i) {
       mbar_init(smem_u32(&sm.q_full[i]), 1);
       mbar_init(smem_u32(&sm.q_empty[i]), 1);
+    }
+    for (int i = 0; i < OSTAGES; ++i) {
+      mbar_init(smem_u32(&sm.o_full[i]), 1);
+      mbar_init(smem_u32(&sm.o_empty[i]), 1);
     }
     mbar_init(smem_u32(&sm.s_full), 1);
     mbar_init(smem_u32(&sm.s_free), 256);
@@ -241,6 +275,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(smem_u32(&sm.tmem_base), TMEM_COLS);
     tmem_relinquish();
   }
+  if (warp == 0) {
+    // the selector operands of the constant products (bf16 1.0 = 0x3F80):
+    // word w of a 16-byte row holds columns 2w, 2w+1
+    const uint32_t wi = lane & 3;
+    const uint32_t sb = wi == 0 ? 0x3F803F80u : (wi == 1 ? 0x00003F80u : 0u);
+    const uint32_t sd = wi == 1 ? 0x3F800000u : (wi == 2 ? 0x3F803F80u : 0u);
+    reinterpret_cast<uint32_t*>(sm.sel[0])[lane] = sb;
+    reinterpret_cast<uint32_t*>(sm.sel[1])[lane] = sd;
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -249,11 +293,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == LOAD_WARP) {
     // -------------------------------------------------------------- producer
     if (lane == 0) {
-      uint32_t it = 0, t = 0;
+      uint32_t it = 0, nq = 0, no = 0;  // K/V, Q and dO loads issued
       bool ok = true;
       Item item;
       for (int x = next_item(p, blockIdx.x, item); x >= 0 && ok;
-           x = next_item(p, x + gridDim.x, item), ++it) {
+           x = next_item(p, x + gridDim.x, item)) {
         const uint32_t slot = it & 1;
         ok = mbar_wait(smem_u32(&sm.kv_empty[slot]), ((it >> 1) & 1) ^ 1, p.limit_ns, abort);
         if (!ok) break;
@@ -261,30 +305,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive_expect_tx(kvb, 2 * TILE_BYTES);
         tma_load_3d(smem_u32(sm.k[slot]), &tmk, kvb, 0, item.kt * BN, item.bh);
         tma_load_3d(smem_u32(sm.v[slot]), &tmv, kvb, 0, item.kt * BN, item.bh);
-        for (int i = 0; i < item.n && ok; ++i, ++t) {
-          const uint32_t st = t & 1;
-          ok = mbar_wait(smem_u32(&sm.q_empty[st]), ((t >> 1) & 1) ^ 1, p.limit_ns, abort);
-          if (!ok) break;
+        ++it;
+        for (int i = 0; i < item.n && ok; ++i) {
           const int qt = item.qt0 + i;
+          const uint32_t st = nq % QSTAGES;
+          ok = mbar_wait(smem_u32(&sm.q_empty[st]), ((nq / QSTAGES) & 1) ^ 1, p.limit_ns, abort);
+          if (!ok) break;
           const uint32_t qb = smem_u32(&sm.q_full[st]);
-          mbar_arrive_expect_tx(qb, 2 * TILE_BYTES + 2 * BM * 4);
+          mbar_arrive_expect_tx(qb, TILE_BYTES + CONST_TILE_BYTES);
           tma_load_3d(smem_u32(sm.q[st]), &tmq, qb, 0, qt * BM, item.bh);
-          tma_load_3d(smem_u32(sm.dout[st]), &tmdo, qb, 0, qt * BM, item.bh);
-          const size_t off = static_cast<size_t>(item.bh) * p.nq_pad + qt * BM;
-          bulk_load(smem_u32(sm.nlse2[st]), p.nlse2 + off, BM * 4, qb);
-          bulk_load(smem_u32(sm.nd[st]), p.nd + off, BM * 4, qb);
+          const size_t tile = static_cast<size_t>(item.bh) * p.num_qt + qt;
+          bulk_load(smem_u32(sm.cst[st]), p.cst + tile * CONST_TILE_BYTES, CONST_TILE_BYTES, qb);
+          ++nq;
+          const uint32_t os = no % OSTAGES;
+          ok = mbar_wait(smem_u32(&sm.o_empty[os]), ((no / OSTAGES) & 1) ^ 1, p.limit_ns, abort);
+          if (!ok) break;
+          const uint32_t ob = smem_u32(&sm.o_full[os]);
+          mbar_arrive_expect_tx(ob, TILE_BYTES);
+          tma_load_3d(smem_u32(sm.dout[os]), &tmdo, ob, 0, qt * BM, item.bh);
+          ++no;
         }
       }
       if (!ok) {
         record_timeout(p, sm);
-        // the copies already issued land before the shared memory goes away
+        // the copies already issued land before the shared memory goes away:
+        // wait (bounded, ignoring the abort flag) for the last phase armed on
+        // every full barrier
         const int never = 0;
         for (uint32_t i = 0; i < 2; ++i) {
-          const uint32_t kv_uses = it / 2 + (i < it % 2 ? 1u : 0u);
-          if (kv_uses > 0)
-            mbar_wait(smem_u32(&sm.kv_full[i]), (kv_uses - 1) & 1, p.limit_ns, &never);
-          const uint32_t q_uses = t / 2 + (i < t % 2 ? 1u : 0u);
-          if (q_uses > 0) mbar_wait(smem_u32(&sm.q_full[i]), (q_uses - 1) & 1, p.limit_ns, &never);
+          const uint32_t uses = it / 2 + (i < it % 2 ? 1u : 0u);
+          if (uses > 0) mbar_wait(smem_u32(&sm.kv_full[i]), (uses - 1) & 1, p.limit_ns, &never);
+        }
+        for (uint32_t i = 0; i < QSTAGES; ++i) {
+          const uint32_t uses = nq / QSTAGES + (i < nq % QSTAGES ? 1u : 0u);
+          if (uses > 0) mbar_wait(smem_u32(&sm.q_full[i]), (uses - 1) & 1, p.limit_ns, &never);
+        }
+        for (uint32_t i = 0; i < OSTAGES; ++i) {
+          const uint32_t uses = no / OSTAGES + (i < no % OSTAGES ? 1u : 0u);
+          if (uses > 0) mbar_wait(smem_u32(&sm.o_full[i]), (uses - 1) & 1, p.limit_ns, &never);
         }
       }
     }
@@ -292,7 +350,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the control flow; one elected lane issues.
     constexpr uint32_t IDESC_SQ = idesc_bf16_f32(BN, BM, false, false);  // S^T, dP^T
-    constexpr uint32_t IDESC_KV = idesc_bf16_f32(BN, D, false, true);    // dV, dK
+    constexpr uint32_t IDESC_KV = idesc_bf16_f32(BN, D, false, true);    // dV (A in tensor memory), dK
     constexpr uint32_t IDESC_DQ = idesc_bf16_f32(BM, D, true, true);     // dQ
     constexpr uint32_t T16 = TILE_BYTES >> 4;                            // a tile in desc units
     // K-major operands (rows x 64 bf16, 8-row groups 1024 B apart; a K step
@@ -301,9 +359,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint64_t kV = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
     const uint64_t kQ = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
     const uint64_t kDO = sdesc_sw128(smem_u32(sm.dout[0]), 16, 1024);
-    // P^T and dS^T as K-major A operands (M = keys, K = queries): a K step
+    // dS^T as the K-major A operand of dK (M = keys, K = queries): a K step
     // inside a 64-query column block is +2, the second block is +16 KB.
-    const uint64_t kPT = sdesc_sw128(smem_u32(sm.pt[0]), 16, 1024);
     const uint64_t kDST = sdesc_sw128(smem_u32(sm.dst[0]), 16, 1024);
     // MN-major B operands (K = the rows of the tile, N = the 64 columns): a K
     // step of 16 rows is +2048 B = +128; 8-row groups 1024 B apart (SBO); N
@@ -314,6 +371,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // dS as the MN-major A operand of dQ (M = queries across the two column
     // blocks, 16 KB apart = LBO; K = keys, 16 rows per step = +128).
     const uint64_t nDS = sdesc_sw128(smem_u32(sm.dst[0]), TILE_BYTES, 1024);
+    // The constant products: A = a selector (every core matrix of the 128 x 16
+    // operand aliases the same 128 bytes: LBO = SBO = 0), B = the Q stage's
+    // [128 queries x 16] constant tile.
+    const uint64_t kSelB = sdesc_plain(smem_u32(sm.sel[0]), 0, 0);
+    const uint64_t kSelD = sdesc_plain(smem_u32(sm.sel[1]), 0, 0);
+    const uint64_t kCst = sdesc_plain(smem_u32(sm.cst[0]), 128, 256);
+    constexpr uint32_t C16 = CONST_TILE_BYTES >> 4;
 
     const bool leader = elect_one();
     bool ok = true;
@@ -327,16 +391,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss(tmem + COL_S, kK + slot * T16 + 2 * kk, kQ + st * T16 + 2 * kk, IDESC_SQ,
                  kk > 0 ? 1u : 0u);
+        mma_ss(tmem + COL_S, kSelB, kCst + st * C16, IDESC_SQ, 1u);  // + b_i
         tc_commit(smem_u32(&sm.s_full));
       }
       __syncwarp();
     };
-    auto issue_dp = [&](uint32_t slot, uint32_t st) {  // dP^T = V dO^T
+    auto issue_dp = [&](uint32_t slot, uint32_t qs, uint32_t os) {  // dP^T = V dO^T
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + COL_DP, kV + slot * T16 + 2 * kk, kDO + st * T16 + 2 * kk, IDESC_SQ,
+          mma_ss(tmem + COL_DP, kV + slot * T16 + 2 * kk, kDO + os * T16 + 2 * kk, IDESC_SQ,
                  kk > 0 ? 1u : 0u);
+        mma_ss(tmem + COL_DP, kSelD, kCst + qs * C16, IDESC_SQ, 1u);  // - D_i
         tc_commit(smem_u32(&sm.dp_full));
       }
       __syncwarp();
@@ -346,26 +412,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     Item cur;
     int cx = next_item(p, blockIdx.x, cur);
     int ci = 0;  // index of tile t inside its item
-    if (cx >= 0 && wait(&sm.kv_full[0], 0) && wait(&sm.q_full[0], 0)) {
+    if (cx >= 0 && wait(&sm.kv_full[0], 0) && wait(&sm.q_full[0], 0) && wait(&sm.o_full[0], 0)) {
       tc_fence_after();
       issue_s(0, 0);
-      issue_dp(0, 0);
+      issue_dp(0, 0, 0);
       while (ok) {
-        const uint32_t slot = it & 1, st = t & 1;
-        // dV += P^T dO (an item's first product overwrites dV, so the
-        // epilogue must have read the previous item's dK and dV)
-        if (ci == 0 && !wait(&sm.dkv_free, (it & 1) ^ 1)) break;
-        if (!wait(&sm.p_full, t & 1)) break;
-        tc_fence_after();
-        if (leader) {
-#pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk)
-            mma_ss(tmem + COL_DV, kPT + (kk >> 2) * T16 + 2 * (kk & 3), nDO + st * T16 + 128 * kk,
-                   IDESC_KV, (ci > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(smem_u32(&sm.p_free));
-        }
-        __syncwarp();
-        // the next tile pair's score products
+        const uint32_t slot = it & 1, st = t % QSTAGES, os = t % OSTAGES;
+        // the next tile pair (possibly of the next item)
         Item nx = cur;
         int nxx = cx, ni = ci + 1;
         uint32_t nit = it;
@@ -375,27 +428,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           nit = it + 1;
         }
         const bool has_next = nxx >= 0;
-        const uint32_t nslot = nit & 1, nst = (t + 1) & 1;
+        const uint32_t nslot = nit & 1, nst = (t + 1) % QSTAGES, nos = (t + 1) % OSTAGES;
+        // its score product goes first, as soon as S'^T of this one is in the
+        // elementwise warps' registers
         if (has_next) {
           if (ni == 0 && !wait(&sm.kv_full[nslot], (nit >> 1) & 1)) break;
-          if (!wait(&sm.q_full[nst], ((t + 1) >> 1) & 1)) break;
+          if (!wait(&sm.q_full[nst], ((t + 1) / QSTAGES) & 1)) break;
           if (!wait(&sm.s_free, t & 1)) break;
           tc_fence_after();
           issue_s(nslot, nst);
         }
+        // dV += P^T dO (an item's first product overwrites dV, so the
+        // epilogue must have read the previous item's dK and dV)
+        if (ci == 0 && !wait(&sm.dkv_free, (it & 1) ^ 1)) break;
+        if (!wait(&sm.p_full, t & 1)) break;
+        tc_fence_after();
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)
+            mma_ts(tmem + COL_DV, tmem + COL_PT + 8 * kk, nDO + os * T16 + 128 * kk, IDESC_KV,
+                   (ci > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(smem_u32(&sm.p_free));
+          tc_commit(smem_u32(&sm.o_empty[os]));  // the last product that reads this dO
+        }
+        __syncwarp();
         if (!wait(&sm.ds_full, t & 1)) break;
         tc_fence_after();
         if (has_next) {
           if (!wait(&sm.dp_free, t & 1)) break;
+          if (!wait(&sm.o_full[nos], ((t + 1) / OSTAGES) & 1)) break;
           tc_fence_after();
-          issue_dp(nslot, nst);
+          issue_dp(nslot, nst, nos);
         }
-        // dK += dS^T Q
+        // dK += dS^T Q (the last product that reads this stage's Q)
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
             mma_ss(tmem + COL_DK, kDST + (kk >> 2) * T16 + 2 * (kk & 3), nQ + st * T16 + 128 * kk,
                    IDESC_KV, (ci > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(smem_u32(&sm.q_empty[st]));
         }
         __syncwarp();
         // dQ = dS K (the epilogue must have read the previous tile's dQ)
@@ -408,7 +479,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                    kk > 0 ? 1u : 0u);
           tc_commit(smem_u32(&sm.dq_full));
           tc_commit(smem_u32(&sm.ds_free));
-          tc_commit(smem_u32(&sm.q_empty[st]));
           if (ci == cur.n - 1) {
             tc_commit(smem_u32(&sm.kv_empty[slot]));
             tc_commit(smem_u32(&sm.dkv_full));
@@ -435,13 +505,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int r = quarter * 32 + lane;  // tensor-memory lane = row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const bool leader = quarter == 0 && lane == 0;
-    const uint32_t stage = smem_u32(sm.stage);
+    const uint32_t stage0 = smem_u32(sm.stage[0]), stage1 = smem_u32(sm.stage[1]);
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, p.limit_ns, abort));
       return ok;
     };
-    // The staging buffer is free once the previous bulk copy has read it.
+    // The two staging buffers are free once the previous bulk copies have
+    // read them; after the rows are written, the copies may start.
     auto stage_acquire = [&]() {
       if (leader) bulk_wait_read_all();
       named_bar_sync(EPI_BAR, 128);
@@ -453,17 +524,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t it = 0, t = 0;
     for (int x = blockIdx.x; x < p.num_items && ok; x += gridDim.x) {
       const Item item = bwd_item(p, x);
-      uint32_t w[32];
       if (item.n == 0) {
         // no query sees these keys: dK = dV = 0
+        uint32_t w[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) w[i] = 0u;
         stage_acquire();
-        st_row_sw128(stage, r, w, 0);
+        st_row_sw128(stage0, r, w, 0);
         stage_release();
         if (leader) {
-          tma_store_3d(&tmdk, stage, 0, item.kt * BN, item.bh);
-          tma_store_3d(&tmdv, stage, 0, item.kt * BN, item.bh);
+          tma_store_3d(&tmdk, stage0, 0, item.kt * BN, item.bh);
+          tma_store_3d(&tmdv, stage0, 0, item.kt * BN, item.bh);
           bulk_commit_group();
         }
         continue;
@@ -482,24 +553,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // two fp32 boxes of 32 columns (128 bytes a row), each added into
         // the accumulator by one TMA reduce; rows past n_q are not touched
         stage_acquire();
-        st_row_sw128(stage, r, a, 0);
+        st_row_sw128(stage0, r, a, 0);
+        st_row_sw128(stage1, r, b, 0);
         stage_release();
         if (leader) {
-          tma_reduce_add_3d(&tmdq, stage, 0, qt * BM, item.bh);
-          bulk_commit_group();
-        }
-        stage_acquire();
-        st_row_sw128(stage, r, b, 0);
-        stage_release();
-        if (leader) {
-          tma_reduce_add_3d(&tmdq, stage, 32, qt * BM, item.bh);
+          tma_reduce_add_3d(&tmdq, stage0, 0, qt * BM, item.bh);
+          tma_reduce_add_3d(&tmdq, stage1, 32, qt * BM, item.bh);
           bulk_commit_group();
         }
       }
       if (!ok || !wait(&sm.dkv_full, it & 1)) break;
       tc_fence_after();
-      // dV, then dK (times the scale), each through the staging buffer; the
+      // dV into staging buffer 0, dK (times the scale) into buffer 1; the
       // accumulators are released once both are in registers
+      stage_acquire();
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         uint32_t a[32], b[32], w[32];
@@ -519,13 +586,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           w[16 + i] =
               pack_bf16x2(__uint_as_float(b[2 * i]) * sc, __uint_as_float(b[2 * i + 1]) * sc);
         }
-        stage_acquire();
-        st_row_sw128(stage, r, w, 0);
-        stage_release();
-        if (leader) {
-          tma_store_3d(which == 0 ? &tmdv : &tmdk, stage, 0, item.kt * BN, item.bh);
-          bulk_commit_group();
-        }
+        st_row_sw128(which == 0 ? stage0 : stage1, r, w, 0);
+      }
+      stage_release();
+      if (leader) {
+        tma_store_3d(&tmdv, stage0, 0, item.kt * BN, item.bh);
+        tma_store_3d(&tmdk, stage1, 0, item.kt * BN, item.bh);
+        bulk_commit_group();
       }
       ++it;
     }
@@ -539,8 +606,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + COL_S + 64 * half;
     const uint32_t tDP = tmem + lane_off + COL_DP + 64 * half;
-    const uint32_t pt_tile = smem_u32(sm.pt[half]);
-    const uint32_t ds_tile = smem_u32(sm.dst[half]);
+    const uint32_t tPT = tmem + lane_off + COL_PT + 32 * half;
     const float c = p.scale_log2;
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -554,7 +620,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int j = item.kt * BN + r;  // this thread's key
       const bool row_valid = j < item.key_limit;
       for (int i = 0; i < item.n; ++i, ++t) {
-        const uint32_t st = t & 1;
         const int qt = item.qt0 + i;
         // leading columns whose query precedes this key (causal diagonal
         // tile), or all of them for a key past the sequence
@@ -564,7 +629,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         } else if (p.mask == kMaskCausal && qt == item.kt) {
           lim = min(max(r - 64 * half, 0), 64);
         }
-        if (!wait(&sm.q_full[st], (t >> 1) & 1)) break;
         if (!wait(&sm.s_full, t & 1)) break;
         tc_fence_after();
         uint32_t s0[32], s1[32];
@@ -575,17 +639,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.s_free));
 
-        // P = 2^(S * scale * log2(e) - LSE * log2(e)), zero where forbidden
-        const uint32_t lse_addr = smem_u32(&sm.nlse2[st][64 * half]);
+        // P = 2^(scale * log2(e) * S') (S' already holds -LSE/scale), zero
+        // where forbidden
         float pf[64];
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {
-          const float4 nl = ld_shared_f4(lse_addr + 16 * g);
-          const uint32_t* src = g < 8 ? s0 + 4 * g : s1 + 4 * (g - 8);
+        for (int i2 = 0; i2 < 32; i2 += 2) {
+          const uint32_t* src = i2 < 16 ? s0 + 2 * i2 : s1 + 2 * (i2 - 16);
           float x0, x1, x2, x3;
-          fma2(x0, x1, __uint_as_float(src[0]), __uint_as_float(src[1]), c, c, nl.x, nl.y);
-          fma2(x2, x3, __uint_as_float(src[2]), __uint_as_float(src[3]), c, c, nl.z, nl.w);
-          const int c0 = 4 * g;
+          fma2(x0, x1, __uint_as_float(src[0]), __uint_as_float(src[1]), c, c, 0.f, 0.f);
+          fma2(x2, x3, __uint_as_float(src[2]), __uint_as_float(src[3]), c, c, 0.f, 0.f);
+          const int c0 = 2 * i2;
           pf[c0 + 0] = c0 + 0 < lim ? 0.f : ex2(x0);
           pf[c0 + 1] = c0 + 1 < lim ? 0.f : ex2(x1);
           pf[c0 + 2] = c0 + 2 < lim ? 0.f : ex2(x2);
@@ -596,17 +659,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int i2 = 0; i2 < 32; ++i2) w[i2] = pack_bf16x2(pf[2 * i2], pf[2 * i2 + 1]);
         // P^T of the previous tile pair has been read by its dV product
         if (!wait(&sm.p_free, (t & 1) ^ 1)) break;
-        st_row_sw128(pt_tile, r, w, 0);
-        fence_proxy_async_smem();
+        tc_fence_after();
+        tmem_st32(tPT, w);
+        tmem_st_wait();
+        tc_fence_before();
         mbar_arrive(smem_u32(&sm.p_full));
 
-        // dS = P * (dP - D), stored 32 columns at a time once dS^T of the
-        // previous tile pair has been read by its dK and dQ products
+        // dS = P * dP' (dP' already holds -D), computed into registers while
+        // the previous tile pair's dK and dQ products still read dS^T
         if (!wait(&sm.dp_full, t & 1)) break;
-        if (!wait(&sm.ds_free, (t & 1) ^ 1)) break;
         tc_fence_after();
-        const uint32_t nd_addr = smem_u32(&sm.nd[st][64 * half]);
-        const uint32_t ds_row = ds_tile + r * 128;
+        uint32_t e[32];  // dS as bf16 pairs, columns 2i, 2i+1
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           uint32_t dp[32];
@@ -617,26 +680,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive(smem_u32(&sm.dp_free));
           }
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {  // 8 columns = one 16-byte chunk
-            uint32_t e[4];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const int cc = 8 * g + 4 * hh;  // column inside the chunk of 32
-              const float4 nd = ld_shared_f4(nd_addr + 128 * h2 + 4 * cc);
-              const int c0 = 32 * h2 + cc;
-              float d0, d1, d2, d3;
-              add2(d0, d1, __uint_as_float(dp[cc]), __uint_as_float(dp[cc + 1]), nd.x, nd.y);
-              add2(d2, d3, __uint_as_float(dp[cc + 2]), __uint_as_float(dp[cc + 3]), nd.z, nd.w);
-              float e0, e1, e2, e3;
-              fma2(e0, e1, pf[c0], pf[c0 + 1], d0, d1, 0.f, 0.f);
-              fma2(e2, e3, pf[c0 + 2], pf[c0 + 3], d2, d3, 0.f, 0.f);
-              e[2 * hh] = pack_bf16x2(e0, e1);
-              e[2 * hh + 1] = pack_bf16x2(e2, e3);
-            }
-            const int chunk = 4 * h2 + g;
-            st_shared_v4(ds_row + ((chunk ^ (r & 7)) << 4), e[0], e[1], e[2], e[3]);
+          for (int cc = 0; cc < 32; cc += 4) {
+            const int c0 = 32 * h2 + cc;
+            float e0, e1, e2, e3;
+            fma2(e0, e1, pf[c0], pf[c0 + 1], __uint_as_float(dp[cc]), __uint_as_float(dp[cc + 1]),
+                 0.f, 0.f);
+            fma2(e2, e3, pf[c0 + 2], pf[c0 + 3], __uint_as_float(dp[cc + 2]),
+                 __uint_as_float(dp[cc + 3]), 0.f, 0.f);
+            e[c0 / 2] = pack_bf16x2(e0, e1);
+            e[c0 / 2 + 1] = pack_bf16x2(e2, e3);
           }
         }
+        if (!wait(&sm.ds_free, (t & 1) ^ 1)) break;
+        st_row_sw128(smem_u32(sm.dst[half]), r, e, 0);
         fence_proxy_async_smem();
         mbar_arrive(smem_u32(&sm.ds_full));
       }
@@ -653,19 +709,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-// Per query row (8 threads a row): -D = -sum_c dO_c O_c, -LSE * log2(e), and
-// the dQ accumulator row set to zero.  Rows n_q .. nq_pad-1 of each head get
-// zeros (their Q and dO rows are zero-filled by the tile loads).
+// x as hi + mid + lo, three bf16 values (each the rounding of what the
+// previous ones leave; together within about 2^-24 of x).
+__device__ __forceinline__ uint2 split3_bf16(float x) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(mid);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+  uint2 w;
+  w.x = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
+        (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16);
+  w.y = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
+  return w;
+}
+
+// Per query row (8 threads a row): D = sum_c dO_c O_c, the constant tile's
+// row for this query (b = -LSE/scale and -D, three bf16 parts each), and the
+// dQ accumulator row set to zero.  Rows n_q .. of the last query tile get zero
+// constants (their Q and dO rows are zero-filled by the tile loads, so every
+// product they enter is zero).
 __global__ void __launch_bounds__(256)
     attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-                        const float* __restrict__ lse, float* __restrict__ nlse2,
-                        float* __restrict__ nd, float* __restrict__ dq_acc, int n_q, int nq_pad,
+                        const float* __restrict__ lse, uint8_t* __restrict__ cst,
+                        float* __restrict__ dq_acc, int n_q, int num_qt, float inv_scale,
                         long long rows) {
   const long long row = static_cast<long long>(blockIdx.x) * 32 + (threadIdx.x >> 3);
   const int sub = threadIdx.x & 7;
   const bool in = row < rows;
-  const long long bh = in ? row / nq_pad : 0;
-  const int i = in ? static_cast<int>(row - bh * nq_pad) : 0;
+  const long long per_head = static_cast<long long>(num_qt) * BM;
+  const long long bh = in ? row / per_head : 0;
+  const int i = in ? static_cast<int>(row - bh * per_head) : 0;  // query index
   const bool valid = in && i < n_q;
   const size_t src = (static_cast<size_t>(bh) * n_q + i) * D + sub * 8;
   float acc = 0.f;
@@ -688,9 +762,23 @@ __global__ void __launch_bounds__(256)
   acc += __shfl_xor_sync(0xffffffffu, acc, 4);
   acc += __shfl_xor_sync(0xffffffffu, acc, 2);
   acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-  if (in && sub == 0) {
-    nd[row] = valid ? -acc : 0.f;
-    nlse2[row] = valid ? -lse[static_cast<size_t>(bh) * n_q + i] * LOG2E : 0.f;
+  if (in && sub < 2) {
+    // sub 0: columns 0-7 of this query's row (b in 0-2, -D in 3-5); sub 1:
+    // columns 8-15, zero
+    const int qt = i / BM, n = i % BM;
+    uint8_t* tile =
+        cst + (static_cast<size_t>(bh) * num_qt + qt) * static_cast<size_t>(CONST_TILE_BYTES);
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (sub == 0 && valid) {
+      const float l = lse[static_cast<size_t>(bh) * n_q + i];
+      const float b = isfinite(l) ? -l * inv_scale : 0.f;  // -inf only for a row that sees no key
+      const uint2 pb = split3_bf16(b);
+      const uint2 pd = split3_bf16(-acc);
+      w.x = pb.x;                         // b_hi, b_mid
+      w.y = pb.y | (pd.x << 16);          // b_lo, -D_hi
+      w.z = (pd.x >> 16) | (pd.y << 16);  // -D_mid, -D_lo
+    }
+    *reinterpret_cast<uint4*>(tile + (n & 7) * 16 + (n >> 3) * 256 + sub * 128) = w;
   }
 }
 
@@ -715,10 +803,9 @@ __global__ void __launch_bounds__(256)
 BwdLayout bwd_layout(int B, int H, int n_q) {
   BwdLayout l;
   const size_t bh = static_cast<size_t>(B) * H;
-  l.nq_pad = (n_q + BM - 1) / BM * BM;
-  l.nlse2_off = 0;
-  l.nd_off = bh * l.nq_pad * 4;
-  l.dq_acc_off = 2 * bh * l.nq_pad * 4;
+  l.num_qt = (n_q + BM - 1) / BM;
+  l.cst_off = 0;
+  l.dq_acc_off = bh * l.num_qt * CONST_TILE_BYTES;
   l.bytes = l.dq_acc_off + bh * static_cast<size_t>(n_q) * D * 4;
   return l;
 }
@@ -729,28 +816,25 @@ cudaError_t launch_bwd(const BwdProblem& pb, const CUtensorMap* maps, void* work
                        const LaunchCtx& ctx) {
   const BwdLayout lay = bwd_layout(pb.B, pb.H, pb.n_q);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* nlse2 = reinterpret_cast<float*>(ws + lay.nlse2_off);
-  float* nd = reinterpret_cast<float*>(ws + lay.nd_off);
+  uint8_t* cst = ws + lay.cst_off;
   float* dq_acc = reinterpret_cast<float*>(ws + lay.dq_acc_off);
   const long long bh = static_cast<long long>(pb.B) * pb.H;
 
-  const long long rows = bh * lay.nq_pad;
+  const long long rows = bh * static_cast<long long>(lay.num_qt) * BM;
   const long long pre_blocks = (rows + 31) / 32;
   attn_bwd_pre_kernel<<<static_cast<unsigned>(pre_blocks), 256, 0, ctx.stream>>>(
       static_cast<const __nv_bfloat16*>(pb.o), static_cast<const __nv_bfloat16*>(pb.dout), pb.lse,
-      nlse2, nd, dq_acc, pb.n_q, static_cast<int>(lay.nq_pad), rows);
+      cst, dq_acc, pb.n_q, static_cast<int>(lay.num_qt), 1.f / pb.scale, rows);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
   Params p;
-  p.nlse2 = nlse2;
-  p.nd = nd;
+  p.cst = cst;
   p.key_lens = pb.key_lens;
   p.H = pb.H;
   p.n_q = pb.n_q;
   p.n_k = pb.n_k;
   p.BH = static_cast<int>(bh);
-  p.nq_pad = static_cast<int>(lay.nq_pad);
   p.mask = pb.mask;
   p.num_qt = (pb.n_q + BM - 1) / BM;
   p.num_kt = (pb.n_k + BN - 1) / BN;

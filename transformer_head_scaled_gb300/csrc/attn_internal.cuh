@@ -88,10 +88,11 @@ struct BwdProblem {
   const int* key_lens;
 };
 
-// Workspace of the backward: -LSE*log2(e) and -D per query row (rows padded
-// to a multiple of 128 per head), then the fp32 dQ accumulator [B, H, n_q, 64].
+// Workspace of the backward: the per-query constant tiles (one [128 x 16]
+// bf16 tile of 4 KB per 128-query tile and head), then the fp32 dQ
+// accumulator [B, H, n_q, 64].
 struct BwdLayout {
-  size_t nq_pad, nlse2_off, nd_off, dq_acc_off, bytes;
+  size_t num_qt, cst_off, dq_acc_off, bytes;
 };
 BwdLayout bwd_layout(int B, int H, int n_q);
 size_t bwd_tc_smem_bytes();

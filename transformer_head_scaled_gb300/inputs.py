@@ -17,6 +17,8 @@ available here; these tensors stand in for them):
 * Per-sequence key lengths for encoder-decoder attention are integers uniform
   on [64, n_k] inclusive, PCG64 seeded 3 (decoding workloads: the filled part
   of each key/value cache, uniform on [lens_lo, n_k]).
+* For the backward, the output gradient dO is i.i.d. N(0, 1), PCG64 seeded 4,
+  rounded to bfloat16 (O and LSE come from the forward on the same inputs).
 * Layout is [B, h, n, d] contiguous (heads split as (h, seq, d)).
 """
 from __future__ import annotations
@@ -31,7 +33,7 @@ MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_KEY_PADDING = 2
 
-SEED_Q, SEED_K, SEED_V, SEED_LENS = 0, 1, 2, 3
+SEED_Q, SEED_K, SEED_V, SEED_LENS, SEED_DOUT = 0, 1, 2, 3, 4
 
 
 @dataclass(frozen=True)
@@ -47,7 +49,8 @@ class Workload:
     mask: int
     dtype: str  # "bf16" or "f32"
     lens_lo: int = 64
-    kind: str = "fwd"  # "fwd": fused forward; "decode": few queries against a cache
+    kind: str = "fwd"  # "fwd": fused forward; "decode": few queries against a cache;
+    #                    "bwd": gradients of the forward
     note: str = field(default="", compare=False)
 
     @property
@@ -82,6 +85,18 @@ WORKLOADS = {
     "decode_long": Workload("decode_long", 32, 16, 1, 4096, 64, MASK_KEY_PADDING, "bf16",
                             lens_lo=2048, kind="decode",
                             note="big model, 8 sentences x beam 4, cache up to 4096"),
+    # Training needs the gradient of every attention layer (section 5 of
+    # "Attention Is All You Need"): the backward on the same problems.
+    "base_enc_bwd": Workload("base_enc_bwd", 64, 8, 512, 512, 64, MASK_NONE, "bf16", kind="bwd",
+                             note="backward of base encoder self-attention"),
+    "base_dec_bwd": Workload("base_dec_bwd", 64, 8, 512, 512, 64, MASK_CAUSAL, "bf16", kind="bwd",
+                             note="backward of base decoder masked self-attention"),
+    "encdec_bwd": Workload("encdec_bwd", 64, 8, 384, 512, 64, MASK_KEY_PADDING, "bf16", kind="bwd",
+                           note="backward of base encoder-decoder attention"),
+    "big_bwd": Workload("big_bwd", 8, 16, 4096, 4096, 64, MASK_NONE, "bf16", kind="bwd",
+                        note="backward, big model, long sequence"),
+    "big_causal_bwd": Workload("big_causal_bwd", 8, 16, 4096, 4096, 64, MASK_CAUSAL, "bf16",
+                               kind="bwd", note="backward, big model, long sequence, causal"),
 }
 
 
@@ -116,10 +131,25 @@ def make_inputs(w: Workload, device="cpu", seeds=(SEED_Q, SEED_K, SEED_V, SEED_L
     return q, k, v, lens
 
 
+def make_dout(w: Workload, device="cpu", seed: int = SEED_DOUT) -> torch.Tensor:
+    """The output gradient dO [B, h, n_q, d] for a backward workload."""
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    g = gaussian((w.B, w.h, w.n_q, w.d), seed).to(dt)
+    return g if device == "cpu" else g.to(device)
+
+
+def products(w: Workload) -> float:
+    """Tile products per pass, in units of one n_q x n_k x d contraction:
+    2 for the forward (Q K^T and P V), 5 for the backward (Q K^T recomputed,
+    dO V^T, P^T dO, dS^T Q, dS K)."""
+    return 5.0 if w.kind == "bwd" else 2.0
+
+
 def flops(w: Workload, key_lens=None) -> float:
-    """Nominal FLOPs of one forward pass: 4*B*h*n_q*n_k*d (two contractions of
-    2*n_q*n_k*d each), halved for the causal mask."""
-    f = 4.0 * w.B * w.h * w.n_q * w.n_k * w.d
+    """Nominal FLOPs of one pass: 2*n_q*n_k*d per contraction and head
+    (forward 4*B*h*n_q*n_k*d, backward 2.5 times that), halved for the causal
+    mask."""
+    f = 2.0 * products(w) * w.B * w.h * w.n_q * w.n_k * w.d
     if w.mask == MASK_CAUSAL:
         f *= 0.5
     return f
@@ -131,18 +161,22 @@ def algorithmic_flops(w: Workload, key_lens=None) -> float:
     if w.mask == MASK_CAUSAL:
         n = min(w.n_q, w.n_k)
         pairs = n * (n + 1) / 2 + max(0, w.n_q - n) * w.n_k
-        return 4.0 * w.B * w.h * pairs * w.d
+        return 2.0 * products(w) * w.B * w.h * pairs * w.d
     if w.mask == MASK_KEY_PADDING:
         lens = np.asarray(key_lens.cpu() if hasattr(key_lens, "cpu") else key_lens)
-        return 4.0 * w.h * w.n_q * float(np.minimum(lens, w.n_k).sum()) * w.d
+        return 2.0 * products(w) * w.h * w.n_q * float(np.minimum(lens, w.n_k).sum()) * w.d
     return flops(w)
 
 
 def hbm_bytes(w: Workload, key_lens=None) -> float:
     """Compulsory HBM bytes of one forward pass: Q, K, V read once, O written
     once, LSE (float32) written once; the n_q x n_k scores never leave the chip.
-    For a decoding step only the filled part of the caches is read."""
+    For a decoding step only the filled part of the caches is read.  The
+    backward reads Q, K, V, O, dO and LSE and writes dQ, dK, dV."""
     es = 2 if w.dtype == "bf16" else 4
+    if w.kind == "bwd":
+        return float(4 * w.B * w.h * w.n_q * w.d * es + 4 * w.B * w.h * w.n_k * w.d * es
+                     + 4 * w.B * w.h * w.n_q)
     qo = 2 * w.B * w.h * w.n_q * w.d * es
     if w.kind == "decode" and key_lens is not None:
         lens = np.asarray(key_lens.cpu() if hasattr(key_lens, "cpu") else key_lens)
