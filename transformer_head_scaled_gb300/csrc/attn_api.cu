@@ -121,12 +121,12 @@ int encode_3d(CUtensorMap* map, const void* base, int d, int n, long long bh, in
   return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
 }
 
-// (64, n, B*H) fp32 view with a (32, 128, 1) box and 128-byte swizzle (the
+// (64, n, B*H) fp32 view with a (32, 64, 1) box and 128-byte swizzle (the
 // backward's dQ accumulator, added into by TMA reduce).
 int encode_3d_f32(CUtensorMap* map, const void* base, int n, long long bh) {
   cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
   cuuint64_t strides[2] = {256u, 256u * static_cast<cuuint64_t>(n)};
-  cuuint32_t box[3] = {32u, 128u, 1u};
+  cuuint32_t box[3] = {32u, 64u, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -323,8 +323,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if ((rc = encode_3d(&maps[1], k, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
   if ((rc = encode_3d(&maps[2], v, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
   if ((rc = encode_3d(&maps[3], dout, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&maps[4], dk, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&maps[5], dv, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&maps[4], dk, d_k, n_k, bh, 64)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&maps[5], dv, d_k, n_k, bh, 64)) != ATTN_OK) return rc;
   if ((rc = encode_3d_f32(&maps[6], static_cast<uint8_t*>(workspace) + lay.dq_acc_off, n_q, bh)) !=
       ATTN_OK)
     return rc;

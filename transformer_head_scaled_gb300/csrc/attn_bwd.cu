@@ -19,7 +19,7 @@
 //      128-key tile of one (b, h); for each 128-query tile that the mask lets
 //      see those keys it runs the tensor-core products of that tile pair and
 //      accumulates dK and dV in tensor memory; dQ of the tile pair is added
-//      into the fp32 accumulator in global memory with a TMA reduce.
+//      into the fp32 accumulator in global memory with TMA reduces.
 //   3. attn_bwd_dq_kernel: dQ = scale * accumulator, rounded to bf16.
 //
 // The per-query constants ride on the tensor cores: one extra K=16 step
@@ -33,12 +33,18 @@
 //   warps 0-7   elementwise: warp w owns tensor-memory lanes 32*(w%4).. (=
 //               keys) and query columns 64*(w/4)..+63; it turns S'^T into P^T
 //               (bf16, written to tensor memory) and dP'^T into dS^T (bf16,
-//               written to shared memory in the 128-byte swizzled layout);
-//   warps 8-11  epilogue: dQ of each tile pair (tensor memory -> swizzled fp32
-//               staging -> TMA reduce-add), dK and dV of each item (-> bf16 ->
-//               TMA store);
-//   warp  12    TMA producer: K, V per item (2 slots); Q, dO and the two
-//               constant tiles per query tile (3 stages);
+//               written to shared memory in the 128-byte swizzled layout, two
+//               buffers so that tile t+1's dS^T is written while dK(t) and
+//               dQ(t) still read tile t's);
+//   warps 8-11  epilogue, two groups of two warps (query or key rows 0-63 and
+//               64-127), each with its own 8 KB staging buffer: dQ of each tile
+//               pair (tensor memory -> swizzled fp32 staging -> TMA reduce-add
+//               into the fp32 accumulator in global memory), dK and dV of each
+//               item (-> bf16 -> TMA store);
+//   warp  12    TMA producer: K per item (2 slots), V per item (1 slot: its
+//               only reader, dP, is done with it a tile pair before the next
+//               item needs it); Q and its constant tile (3 stages) and dO (2
+//               stages) per query tile;
 //   warp  13    tensor-memory owner and MMA issuer.
 // Tensor memory (512 columns): S'^T [0,128)  dP'^T [128,256)  dV [256,320)
 // dK [320,384)  dQ [384,448)  P^T [448,512) (bf16 pairs).  Keys are the 128
@@ -81,29 +87,34 @@ constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 320, COL_DQ =
 // 8-row groups 256 B apart).  Row i holds b_i in columns 0-2 (hi, mid, lo)
 // and -D_i in columns 3-5; columns 6-15 are zero.
 constexpr uint32_t CONST_TILE_BYTES = 128 * 16 * 2;
-constexpr int EPI_BAR = 1;  // named barrier of the 128 epilogue threads
 constexpr float LOG2E = 1.4426950408889634f;
 
 static_assert(BM == BN, "the causal tile range assumes square tiles");
 
+constexpr uint32_t HALF_TILE_BYTES = TILE_BYTES / 2;  // 64 rows x 128 bytes
+constexpr int EPI_BAR0 = 1;  // named barriers 1, 2: the two epilogue groups
+
 struct __align__(1024) Smem {
   uint8_t k[2][TILE_BYTES];
-  uint8_t v[2][TILE_BYTES];
+  uint8_t v[TILE_BYTES];
   uint8_t q[QSTAGES][TILE_BYTES];
   uint8_t dout[OSTAGES][TILE_BYTES];
-  // dS^T as [128 keys x 128 queries] bf16: two 64-query column blocks of
-  // [128 x 64], each in the 128-byte swizzled layout.
-  uint8_t dst[2][TILE_BYTES];
-  uint8_t stage[2][TILE_BYTES];  // epilogue staging (the two fp32 halves of dQ, or dV and dK)
+  // dS^T as [128 keys x 128 queries] bf16, two buffers (tile pairs t even /
+  // odd), each two 64-query column blocks of [128 x 64] in the 128-byte
+  // swizzled layout.
+  uint8_t dst[2][2][TILE_BYTES];
+  // epilogue staging, one 64-row buffer per epilogue group: a 32-column fp32
+  // half of dQ, or dV / dK in bf16, 128-byte swizzled
+  uint8_t stage[2][HALF_TILE_BYTES];
   uint8_t cst[QSTAGES][CONST_TILE_BYTES];  // the constant tile of each Q stage
   // Two 8 x 8 bf16 core matrices that select columns of the constant tile:
   // [0] rows (1,1,1,0,0,0,0,0) picks b, [1] rows (0,0,0,1,1,1,0,0) picks -D.
   uint8_t sel[2][512];
-  uint64_t kv_full[2], kv_empty[2];
+  uint64_t k_full[2], k_empty[2], v_full, v_empty;
   uint64_t q_full[QSTAGES], q_empty[QSTAGES];
   uint64_t o_full[OSTAGES], o_empty[OSTAGES];
   uint64_t s_full, s_free, dp_full, dp_free;
-  uint64_t p_full, p_free, ds_full, ds_free;
+  uint64_t p_full, p_free, ds_full, ds_free[2];
   uint64_t dq_full, dq_free, dkv_full, dkv_free;
   uint64_t drain;
   uint32_t tmem_base;
@@ -111,7 +122,7 @@ struct __align__(1024) Smem {
 };
 
 struct Params {
-  const uint8_t* cst;  // constant tiles [BH][num_qt][2][CONST_TILE_BYTES]
+  const uint8_t* cst;  // constant tiles [BH][num_qt][CONST_TILE_BYTES]
   const int* key_lens;
   int H, n_q, n_k, BH;
   int mask;
@@ -173,6 +184,9 @@ __device__ __forceinline__ void record_timeout(const Params& p, Smem& sm) {
   *reinterpret_cast<volatile int*>(&sm.abort) = 1;
 }
 
+// 3-D tiled reduce-add shared -> global (fp32 add, element type from the
+// tensor map), tracked by the issuing thread's bulk groups.  Parts of the box
+// outside the tensor are not touched.
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int x,
                                                   int y, int z) {
   asm volatile(
@@ -235,9 +249,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&sm.kv_full[i]), 1);
-      mbar_init(smem_u32(&sm.kv_empty[i]), 1);
+      mbar_init(smem_u32(&sm.k_full[i]), 1);
+      mbar_init(smem_u32(&sm.k_empty[i]), 1);
     }
+    mbar_init(smem_u32(&sm.v_full), 1);
+    mbar_init(smem_u32(&sm.v_empty), 1);
     for (int i = 0; i < QSTAGES; ++i) {
       mbar_init(smem_u32(&sm.q_full[i]), 1);
       mbar_init(smem_u32(&sm.q_empty[i]), 1);
@@ -253,7 +269,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(smem_u32(&sm.p_full), 256);
     mbar_init(smem_u32(&sm.p_free), 1);
     mbar_init(smem_u32(&sm.ds_full), 256);
-    mbar_init(smem_u32(&sm.ds_free), 1);
+    mbar_init(smem_u32(&sm.ds_free[0]), 1);
+    mbar_init(smem_u32(&sm.ds_free[1]), 1);
     mbar_init(smem_u32(&sm.dq_full), 1);
     mbar_init(smem_u32(&sm.dq_free), 128);
     mbar_init(smem_u32(&sm.dkv_full), 1);
@@ -293,18 +310,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == LOAD_WARP) {
     // -------------------------------------------------------------- producer
     if (lane == 0) {
-      uint32_t it = 0, nq = 0, no = 0;  // K/V, Q and dO loads issued
+      uint32_t it = 0, nv = 0, nq = 0, no = 0;  // K, V, Q and dO loads issued
       bool ok = true;
       Item item;
       for (int x = next_item(p, blockIdx.x, item); x >= 0 && ok;
            x = next_item(p, x + gridDim.x, item)) {
         const uint32_t slot = it & 1;
-        ok = mbar_wait(smem_u32(&sm.kv_empty[slot]), ((it >> 1) & 1) ^ 1, p.limit_ns, abort);
+        ok = mbar_wait(smem_u32(&sm.k_empty[slot]), ((it >> 1) & 1) ^ 1, p.limit_ns, abort);
         if (!ok) break;
-        const uint32_t kvb = smem_u32(&sm.kv_full[slot]);
-        mbar_arrive_expect_tx(kvb, 2 * TILE_BYTES);
-        tma_load_3d(smem_u32(sm.k[slot]), &tmk, kvb, 0, item.kt * BN, item.bh);
-        tma_load_3d(smem_u32(sm.v[slot]), &tmv, kvb, 0, item.kt * BN, item.bh);
+        mbar_arrive_expect_tx(smem_u32(&sm.k_full[slot]), TILE_BYTES);
+        tma_load_3d(smem_u32(sm.k[slot]), &tmk, smem_u32(&sm.k_full[slot]), 0, item.kt * BN,
+                    item.bh);
         ++it;
         for (int i = 0; i < item.n && ok; ++i) {
           const int qt = item.qt0 + i;
@@ -317,6 +333,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const size_t tile = static_cast<size_t>(item.bh) * p.num_qt + qt;
           bulk_load(smem_u32(sm.cst[st]), p.cst + tile * CONST_TILE_BYTES, CONST_TILE_BYTES, qb);
           ++nq;
+          if (i == 0) {
+            // V of this item, once the previous item's last dP has read the slot
+            ok = mbar_wait(smem_u32(&sm.v_empty), (nv & 1) ^ 1, p.limit_ns, abort);
+            if (!ok) break;
+            mbar_arrive_expect_tx(smem_u32(&sm.v_full), TILE_BYTES);
+            tma_load_3d(smem_u32(sm.v), &tmv, smem_u32(&sm.v_full), 0, item.kt * BN, item.bh);
+            ++nv;
+          }
           const uint32_t os = no % OSTAGES;
           ok = mbar_wait(smem_u32(&sm.o_empty[os]), ((no / OSTAGES) & 1) ^ 1, p.limit_ns, abort);
           if (!ok) break;
@@ -332,18 +356,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // wait (bounded, ignoring the abort flag) for the last phase armed on
         // every full barrier
         const int never = 0;
-        for (uint32_t i = 0; i < 2; ++i) {
-          const uint32_t uses = it / 2 + (i < it % 2 ? 1u : 0u);
-          if (uses > 0) mbar_wait(smem_u32(&sm.kv_full[i]), (uses - 1) & 1, p.limit_ns, &never);
-        }
-        for (uint32_t i = 0; i < QSTAGES; ++i) {
-          const uint32_t uses = nq / QSTAGES + (i < nq % QSTAGES ? 1u : 0u);
-          if (uses > 0) mbar_wait(smem_u32(&sm.q_full[i]), (uses - 1) & 1, p.limit_ns, &never);
-        }
-        for (uint32_t i = 0; i < OSTAGES; ++i) {
-          const uint32_t uses = no / OSTAGES + (i < no % OSTAGES ? 1u : 0u);
-          if (uses > 0) mbar_wait(smem_u32(&sm.o_full[i]), (uses - 1) & 1, p.limit_ns, &never);
-        }
+        auto drain = [&](uint64_t* full, uint32_t stages, uint32_t issued) {
+          for (uint32_t i = 0; i < stages; ++i) {
+            const uint32_t uses = issued / stages + (i < issued % stages ? 1u : 0u);
+            if (uses > 0) mbar_wait(smem_u32(&full[i]), (uses - 1) & 1, p.limit_ns, &never);
+          }
+        };
+        drain(sm.k_full, 2, it);
+        drain(&sm.v_full, 1, nv);
+        drain(sm.q_full, QSTAGES, nq);
+        drain(sm.o_full, OSTAGES, no);
       }
     }
   } else if (warp == MMA_WARP) {
@@ -356,12 +378,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // K-major operands (rows x 64 bf16, 8-row groups 1024 B apart; a K step
     // of 16 elements is +32 B = +2 inside the swizzle row).
     const uint64_t kK = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
-    const uint64_t kV = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);
+    const uint64_t kV = sdesc_sw128(smem_u32(sm.v), 16, 1024);
     const uint64_t kQ = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
     const uint64_t kDO = sdesc_sw128(smem_u32(sm.dout[0]), 16, 1024);
     // dS^T as the K-major A operand of dK (M = keys, K = queries): a K step
     // inside a 64-query column block is +2, the second block is +16 KB.
-    const uint64_t kDST = sdesc_sw128(smem_u32(sm.dst[0]), 16, 1024);
+    const uint64_t kDST = sdesc_sw128(smem_u32(sm.dst[0][0]), 16, 1024);
     // MN-major B operands (K = the rows of the tile, N = the 64 columns): a K
     // step of 16 rows is +2048 B = +128; 8-row groups 1024 B apart (SBO); N
     // is one swizzle atom, LBO unused (set to 1024).
@@ -370,7 +392,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint64_t nK = sdesc_sw128(smem_u32(sm.k[0]), 1024, 1024);
     // dS as the MN-major A operand of dQ (M = queries across the two column
     // blocks, 16 KB apart = LBO; K = keys, 16 rows per step = +128).
-    const uint64_t nDS = sdesc_sw128(smem_u32(sm.dst[0]), TILE_BYTES, 1024);
+    const uint64_t nDS = sdesc_sw128(smem_u32(sm.dst[0][0]), TILE_BYTES, 1024);
     // The constant products: A = a selector (every core matrix of the 128 x 16
     // operand aliases the same 128 bytes: LBO = SBO = 0), B = the Q stage's
     // [128 queries x 16] constant tile.
@@ -396,14 +418,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       __syncwarp();
     };
-    auto issue_dp = [&](uint32_t slot, uint32_t qs, uint32_t os) {  // dP^T = V dO^T
+    // dP^T = V dO^T; the last tile pair of an item releases the V slot
+    auto issue_dp = [&](uint32_t qs, uint32_t os, bool last_of_item) {
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + COL_DP, kV + slot * T16 + 2 * kk, kDO + os * T16 + 2 * kk, IDESC_SQ,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(tmem + COL_DP, kV + 2 * kk, kDO + os * T16 + 2 * kk, IDESC_SQ, kk > 0 ? 1u : 0u);
         mma_ss(tmem + COL_DP, kSelD, kCst + qs * C16, IDESC_SQ, 1u);  // - D_i
         tc_commit(smem_u32(&sm.dp_full));
+        if (last_of_item) tc_commit(smem_u32(&sm.v_empty));
       }
       __syncwarp();
     };
@@ -412,10 +435,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     Item cur;
     int cx = next_item(p, blockIdx.x, cur);
     int ci = 0;  // index of tile t inside its item
-    if (cx >= 0 && wait(&sm.kv_full[0], 0) && wait(&sm.q_full[0], 0) && wait(&sm.o_full[0], 0)) {
+    if (cx >= 0 && wait(&sm.k_full[0], 0) && wait(&sm.q_full[0], 0) && wait(&sm.v_full, 0) &&
+        wait(&sm.o_full[0], 0)) {
       tc_fence_after();
       issue_s(0, 0);
-      issue_dp(0, 0, 0);
+      issue_dp(0, 0, cur.n == 1);
       while (ok) {
         const uint32_t slot = it & 1, st = t % QSTAGES, os = t % OSTAGES;
         // the next tile pair (possibly of the next item)
@@ -432,7 +456,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // its score product goes first, as soon as S'^T of this one is in the
         // elementwise warps' registers
         if (has_next) {
-          if (ni == 0 && !wait(&sm.kv_full[nslot], (nit >> 1) & 1)) break;
+          if (ni == 0 && !wait(&sm.k_full[nslot], (nit >> 1) & 1)) break;
           if (!wait(&sm.q_full[nst], ((t + 1) / QSTAGES) & 1)) break;
           if (!wait(&sm.s_free, t & 1)) break;
           tc_fence_after();
@@ -456,16 +480,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         if (has_next) {
           if (!wait(&sm.dp_free, t & 1)) break;
+          if (ni == 0 && !wait(&sm.v_full, nit & 1)) break;
           if (!wait(&sm.o_full[nos], ((t + 1) / OSTAGES) & 1)) break;
           tc_fence_after();
-          issue_dp(nslot, nst, nos);
+          issue_dp(nst, nos, ni == nx.n - 1);
         }
         // dK += dS^T Q (the last product that reads this stage's Q)
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
-            mma_ss(tmem + COL_DK, kDST + (kk >> 2) * T16 + 2 * (kk & 3), nQ + st * T16 + 128 * kk,
-                   IDESC_KV, (ci > 0 || kk > 0) ? 1u : 0u);
+            mma_ss(tmem + COL_DK, kDST + (2 * (t & 1) + (kk >> 2)) * T16 + 2 * (kk & 3),
+                   nQ + st * T16 + 128 * kk, IDESC_KV, (ci > 0 || kk > 0) ? 1u : 0u);
           tc_commit(smem_u32(&sm.q_empty[st]));
         }
         __syncwarp();
@@ -475,12 +500,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ss(tmem + COL_DQ, nDS + 128 * kk, nK + slot * T16 + 128 * kk, IDESC_DQ,
-                   kk > 0 ? 1u : 0u);
+            mma_ss(tmem + COL_DQ, nDS + 2 * (t & 1) * T16 + 128 * kk, nK + slot * T16 + 128 * kk,
+                   IDESC_DQ, kk > 0 ? 1u : 0u);
           tc_commit(smem_u32(&sm.dq_full));
-          tc_commit(smem_u32(&sm.ds_free));
+          tc_commit(smem_u32(&sm.ds_free[t & 1]));
           if (ci == cur.n - 1) {
-            tc_commit(smem_u32(&sm.kv_empty[slot]));
+            tc_commit(smem_u32(&sm.k_empty[slot]));
             tc_commit(smem_u32(&sm.dkv_full));
           }
         }
@@ -504,37 +529,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // tensor-memory lane = row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const bool leader = quarter == 0 && lane == 0;
-    const uint32_t stage0 = smem_u32(sm.stage[0]), stage1 = smem_u32(sm.stage[1]);
+    // group g = rows 64g .. 64g+63 (warps 8+2g, 9+2g), staging buffer g
+    const int g = quarter >> 1;
+    const int rg = r & 63;  // row inside the group's 64-row box
+    const bool leader = (quarter & 1) == 0 && lane == 0;
+    const uint32_t stage = smem_u32(sm.stage[g]);
+    const uint32_t bar_id = EPI_BAR0 + g;
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) {
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), parity, p.limit_ns, abort));
       return ok;
     };
-    // The two staging buffers are free once the previous bulk copies have
-    // read them; after the rows are written, the copies may start.
+    // The group's buffer is free once its previous bulk copy has read it;
+    // after the rows are written, the copy may start.
     auto stage_acquire = [&]() {
       if (leader) bulk_wait_read_all();
-      named_bar_sync(EPI_BAR, 128);
+      named_bar_sync(bar_id, 64);
     };
     auto stage_release = [&]() {
       fence_proxy_async_smem();
-      named_bar_sync(EPI_BAR, 128);
+      named_bar_sync(bar_id, 64);
     };
     uint32_t it = 0, t = 0;
     for (int x = blockIdx.x; x < p.num_items && ok; x += gridDim.x) {
       const Item item = bwd_item(p, x);
+      const int key_row0 = item.kt * BN + 64 * g;
       if (item.n == 0) {
         // no query sees these keys: dK = dV = 0
         uint32_t w[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) w[i] = 0u;
         stage_acquire();
-        st_row_sw128(stage0, r, w, 0);
+        st_row_sw128(stage, rg, w, 0);
         stage_release();
-        if (leader) {
-          tma_store_3d(&tmdk, stage0, 0, item.kt * BN, item.bh);
-          tma_store_3d(&tmdv, stage0, 0, item.kt * BN, item.bh);
+        if (leader && key_row0 < p.n_k) {
+          tma_store_3d(&tmdk, stage, 0, key_row0, item.bh);
+          tma_store_3d(&tmdv, stage, 0, key_row0, item.bh);
           bulk_commit_group();
         }
         continue;
@@ -549,24 +579,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         reg_fence(b);
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.dq_free));
-        const int qt = item.qt0 + i;
-        // two fp32 boxes of 32 columns (128 bytes a row), each added into
+        // two fp32 boxes of 32 columns x 64 rows per group, each added into
         // the accumulator by one TMA reduce; rows past n_q are not touched
+        const int q_row0 = (item.qt0 + i) * BM + 64 * g;
         stage_acquire();
-        st_row_sw128(stage0, r, a, 0);
-        st_row_sw128(stage1, r, b, 0);
+        st_row_sw128(stage, rg, a, 0);
         stage_release();
-        if (leader) {
-          tma_reduce_add_3d(&tmdq, stage0, 0, qt * BM, item.bh);
-          tma_reduce_add_3d(&tmdq, stage1, 32, qt * BM, item.bh);
+        if (leader && q_row0 < p.n_q) {
+          tma_reduce_add_3d(&tmdq, stage, 0, q_row0, item.bh);
+          bulk_commit_group();
+        }
+        stage_acquire();
+        st_row_sw128(stage, rg, b, 0);
+        stage_release();
+        if (leader && q_row0 < p.n_q) {
+          tma_reduce_add_3d(&tmdq, stage, 32, q_row0, item.bh);
           bulk_commit_group();
         }
       }
       if (!ok || !wait(&sm.dkv_full, it & 1)) break;
       tc_fence_after();
-      // dV into staging buffer 0, dK (times the scale) into buffer 1; the
-      // accumulators are released once both are in registers
-      stage_acquire();
+      // dV, then dK (times the scale); the accumulators are released once
+      // both are in registers
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         uint32_t a[32], b[32], w[32];
@@ -586,13 +620,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           w[16 + i] =
               pack_bf16x2(__uint_as_float(b[2 * i]) * sc, __uint_as_float(b[2 * i + 1]) * sc);
         }
-        st_row_sw128(which == 0 ? stage0 : stage1, r, w, 0);
-      }
-      stage_release();
-      if (leader) {
-        tma_store_3d(&tmdv, stage0, 0, item.kt * BN, item.bh);
-        tma_store_3d(&tmdk, stage1, 0, item.kt * BN, item.bh);
-        bulk_commit_group();
+        stage_acquire();
+        st_row_sw128(stage, rg, w, 0);
+        stage_release();
+        if (leader && key_row0 < p.n_k) {
+          tma_store_3d(which == 0 ? &tmdv : &tmdk, stage, 0, key_row0, item.bh);
+          bulk_commit_group();
+        }
       }
       ++it;
     }
@@ -691,8 +725,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             e[c0 / 2 + 1] = pack_bf16x2(e2, e3);
           }
         }
-        if (!wait(&sm.ds_free, (t & 1) ^ 1)) break;
-        st_row_sw128(smem_u32(sm.dst[half]), r, e, 0);
+        // dS^T buffer t % 2 was last read by the products of tile pair t - 2
+        if (!wait(&sm.ds_free[t & 1], ((t >> 1) & 1) ^ 1)) break;
+        st_row_sw128(smem_u32(sm.dst[t & 1][half]), r, e, 0);
         fence_proxy_async_smem();
         mbar_arrive(smem_u32(&sm.ds_full));
       }

@@ -96,9 +96,10 @@ struct BwdLayout {
 };
 BwdLayout bwd_layout(int B, int H, int n_q);
 size_t bwd_tc_smem_bytes();
-// maps: Q, K, V, dO, dK, dV as 3-D (64, n, B*H) bf16 with a (64, 128, 1) box,
-// then the dQ accumulator as 3-D (64, n_q, B*H) fp32 with a (32, 128, 1) box;
-// all with 128-byte swizzle.  Three launches (preprocess, main, dQ convert).
+// maps: Q, K, V, dO as 3-D (64, n, B*H) bf16 with a (64, 128, 1) box; dK, dV
+// the same with a (64, 64, 1) box; the dQ accumulator as 3-D (64, n_q, B*H)
+// fp32 with a (32, 64, 1) box; all with 128-byte swizzle.  Three launches
+// (preprocess, main, dQ convert).
 cudaError_t launch_bwd(const BwdProblem& pb, const CUtensorMap* maps, void* workspace,
                        const LaunchCtx& ctx);
 
