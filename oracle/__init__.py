@@ -71,6 +71,11 @@ def _load():
             h.restype = ctypes.c_int
             h.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_long] * 6 + [
                 ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
+            bd = lib.oracle_attn_band_f64
+            bd.restype = ctypes.c_int
+            bd.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_long] * 6 + [
+                ctypes.c_double, ctypes.c_long, ctypes.c_long, ctypes.c_void_p, ctypes.c_long,
+                ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -166,3 +171,29 @@ def attn_bwd(q, k, v, dout, scale: float, mask_kind: int = MASK_NONE, key_lens=N
     if rc != 0:
         raise RuntimeError(f"oracle_attn_bwd_f64 failed ({rc})")
     return dq, dk, dv
+
+
+def attn_band(q, k, v, scale: float, left: int, right: int, rows=None, threads: int = 0):
+    """Restricted self-attention: query i sees keys i-left <= j <= i+right.
+
+    Every row (o [B,H,n_q,d_v], lse [B,H,n_q]) or, with ``rows``, only those
+    flat rows (o [len(rows), d_v], lse [len(rows)]), float64.
+    """
+    q, k, v, _, (B, H, n_q, n_k, d_k, d_v) = _prep(q, k, v, MASK_NONE, None)
+    if left < 0 or right < 0:
+        raise ValueError("window sides must be >= 0")
+    if rows is None:
+        o = np.empty((B, H, n_q, d_v), dtype=np.float64)
+        lse = np.empty((B, H, n_q), dtype=np.float64)
+        rp, nr = None, 0
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        o = np.empty((rows.size, d_v), dtype=np.float64)
+        lse = np.empty((rows.size,), dtype=np.float64)
+        rp, nr = rows.ctypes.data, rows.size
+    rc = _load().oracle_attn_band_f64(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, n_q, n_k, d_k, d_v, float(scale),
+        int(left), int(right), rp, nr, int(threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_band_f64 failed ({rc})")
+    return o, lse

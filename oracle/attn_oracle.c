@@ -305,3 +305,87 @@ int oracle_attn_bwd_f64(const float* q, const float* k, const float* v, const fl
   (void)n_threads;
   return failed ? -2 : 0;
 }
+
+/*
+ * Restricted self-attention ("Lire << Attention Is All You Need >>", section
+ * 4 and Table 1; the slide deck "Attention Is All You Need", Table 1: each
+ * output position attends only to a neighbourhood of the input positions
+ * around it).  Query i sees the keys j with  i - left <= j <= i + right
+ * (left = right = w: a window of 2w + 1 positions centred on i; right = 0: a
+ * causal window of the left + 1 most recent positions); every other
+ * connection is -inf before the softmax.  Same definition otherwise as
+ * oracle_row; a row with no key in its window gets o = 0, lse = -inf.
+ */
+static void oracle_band_row(const float* q, const float* k, const float* v, double* oi,
+                            double* lse_i, long H, long n_q, long n_k, long d_k, long d_v,
+                            double scale, long left, long right, long row, double* s) {
+  long i = row % n_q;
+  long bh = row / n_q;
+  (void)H;
+  const float* qi = q + (bh * n_q + i) * d_k;
+  const float* kb = k + bh * n_k * d_k;
+  const float* vb = v + bh * n_k * d_v;
+  double m = -INFINITY;
+  for (long j = 0; j < n_k; ++j) {
+    int forbidden = (j < i - left) || (j > i + right);
+    if (forbidden) {
+      s[j] = -INFINITY;
+      continue;
+    }
+    double dot = 0.0;
+    for (long t = 0; t < d_k; ++t) dot += (double)qi[t] * (double)kb[j * d_k + t];
+    s[j] = scale * dot;
+    if (s[j] > m) m = s[j];
+  }
+  for (long c = 0; c < d_v; ++c) oi[c] = 0.0;
+  if (m == -INFINITY) {
+    *lse_i = -INFINITY;
+    return;
+  }
+  double Z = 0.0;
+  for (long j = 0; j < n_k; ++j) {
+    if (s[j] == -INFINITY) continue;
+    double w = exp(s[j] - m);
+    Z += w;
+    for (long c = 0; c < d_v; ++c) oi[c] += w * (double)vb[j * d_v + c];
+  }
+  for (long c = 0; c < d_v; ++c) oi[c] /= Z;
+  *lse_i = m + log(Z);
+}
+
+/* Every row, or (rows != NULL) only the listed flat rows (b*H + h)*n_q + i.
+ * left, right >= 0.  Returns 0, -1 on bad arguments, -2 when scratch cannot
+ * be allocated. */
+int oracle_attn_band_f64(const float* q, const float* k, const float* v, double* o, double* lse,
+                         long B, long H, long n_q, long n_k, long d_k, long d_v, double scale,
+                         long left, long right, const long* rows, long n_rows, int n_threads) {
+  if (B < 0 || H < 0 || n_q < 1 || n_k < 1 || d_k < 1 || d_v < 1 || left < 0 || right < 0)
+    return -1;
+  const long total = rows ? n_rows : B * H * n_q;
+  int failed = 0;
+#ifdef _OPENMP
+  if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel
+#endif
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)n_k);
+    if (s == NULL) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+      failed = 1;
+    } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 64)
+#endif
+      for (long x = 0; x < total; ++x) {
+        long row = rows ? rows[x] : x;
+        oracle_band_row(q, k, v, o + x * d_v, lse + x, H, n_q, n_k, d_k, d_v, scale, left, right,
+                        row, s);
+      }
+      free(s);
+    }
+  }
+  (void)n_threads;
+  return failed ? -2 : 0;
+}
