@@ -170,7 +170,8 @@ def dist_env():
 
 
 def workload_desc(w: inputs.Workload) -> str:
-    mask = {0: "no mask", 1: "causal", 2: "key padding L~U[64,n_k]"}[w.mask]
+    mask = {0: "no mask", 1: "causal", 2: "key padding L~U[64,n_k]",
+            3: f"window i-{w.win_left}..i+{w.win_right}"}[w.mask]
     return f"{w.name}: B={w.B} h={w.h} n_q={w.n_q} n_k={w.n_k} d_k=d_v={w.d} {w.dtype} {mask}"
 
 
@@ -181,9 +182,19 @@ def _row_flops(w: inputs.Workload, rows, lens) -> float:
         keys = np.full(rows.size, w.n_k)
     elif w.mask == inputs.MASK_CAUSAL:
         keys = np.minimum(rows % w.n_q + 1, w.n_k)
+    elif w.mask == inputs.MASK_BAND:
+        i = rows % w.n_q
+        keys = np.maximum(np.minimum(w.n_k - 1, i + w.win_right) - np.maximum(0, i - w.win_left) + 1, 0)
     else:
         keys = np.minimum(lens[(rows // w.n_q) // w.h], w.n_k)
     return float(4.0 * w.d * keys.sum())
+
+
+def _oracle_rows(oracle, w, q, k, v, rows, kl, threads):
+    if w.mask == inputs.MASK_BAND:
+        return oracle.attn_band(q, k, v, w.scale, w.win_left, w.win_right, rows=rows,
+                                threads=threads)
+    return oracle.attn_rows(q, k, v, rows, w.scale, w.mask, kl, threads=threads)
 
 
 def oracle_sample(w: inputs.Workload, q, k, v, kl, target_s: float, threads: int = 0,
@@ -200,7 +211,7 @@ def oracle_sample(w: inputs.Workload, q, k, v, kl, target_s: float, threads: int
         n = min(total_rows, 1024)
         rows = np.sort(rng.choice(total_rows, size=n, replace=False))
         t0 = time.perf_counter()
-        oracle.attn_rows(q, k, v, rows, w.scale, w.mask, kl, threads=threads)
+        _oracle_rows(oracle, w, q, k, v, rows, kl, threads)
         per_row = (time.perf_counter() - t0) / n
         rows_hint = max(1, int(target_s / max(per_row, 1e-9)))
     done, flops, dt = 0, 0.0, 0.0
@@ -209,7 +220,7 @@ def oracle_sample(w: inputs.Workload, q, k, v, kl, target_s: float, threads: int
         rows = (np.arange(total_rows, dtype=np.int64) if n == total_rows
                 else np.sort(rng.choice(total_rows, size=n, replace=False)))
         t0 = time.perf_counter()
-        oracle.attn_rows(q, k, v, rows, w.scale, w.mask, kl, threads=threads)
+        _oracle_rows(oracle, w, q, k, v, rows, kl, threads)
         dt += time.perf_counter() - t0
         flops += _row_flops(w, rows, lens)
         done += n
@@ -356,6 +367,9 @@ def run_ours(args, w):
         elif bwd:
             rc = binding.attn_bwd_raw(*bptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale, w.mask, klp,
                                       ws.data_ptr(), ws_bytes, sptr)
+        elif w.mask == inputs.MASK_BAND:
+            rc = binding.attn_fwd_window_raw(*ptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale,
+                                             w.win_left, w.win_right, sptr)
         else:
             rc = binding.attn_fwd_raw(*ptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale, w.mask, klp,
                                       sptr, f32=f32)
@@ -483,6 +497,10 @@ def run_e2e(args, w, q, k, v, kl, dev, stream, f32):
                                          do.data_ptr(), dl.data_ptr(), w.B, w.h, w.n_q, w.n_k,
                                          w.d, w.scale, None if dkl is None else dkl.data_ptr(),
                                          ws.data_ptr(), ws_bytes, sptr)
+        elif w.mask == inputs.MASK_BAND:
+            rc = binding.attn_fwd_window_raw(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                             do.data_ptr(), dl.data_ptr(), w.B, w.h, w.n_q, w.n_k,
+                                             w.d, w.scale, w.win_left, w.win_right, sptr)
         else:
             rc = binding.attn_fwd_raw(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(),
                                       dl.data_ptr(), w.B, w.h, w.n_q, w.n_k, w.d, w.scale,

@@ -79,6 +79,23 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              struct CUstream_st* stream);
 
 /*
+ * attn_fwd_window -- attn_fwd with restricted self-attention: query i sees
+ * the keys j with  i - window_left <= j <= i + window_right  (and j < n_k),
+ * every other connection is -inf before the softmax.  window_left =
+ * window_right = w gives the neighbourhood of 2w + 1 positions centred on
+ * the output position that "Attention Is All You Need" proposes for very
+ * long sequences (section 4 and Table 1: O(r n d) work instead of O(n^2 d));
+ * window_right = 0 gives a causal window of window_left + 1 positions.
+ * Tiles outside every row's window are never loaded.  Arguments otherwise as
+ * attn_fwd (bf16, d_k = 64); window_left, window_right >= 0
+ * (ATTN_ERR_INVALID_ARG otherwise).  A query whose window holds no key
+ * (i - window_left >= n_k) gets O = 0, LSE = -inf.
+ */
+int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+                    int n_q, int n_k, int d_k, float scale, int window_left, int window_right,
+                    struct CUstream_st* stream);
+
+/*
  * attn_fwd_f32 -- float32 forward on the CUDA cores (fp32 FMA, same
  * definition, same arguments with float tensors).  d_k in {16, 32, 64, 128}.
  */

@@ -154,3 +154,14 @@ def test_bwd_workspace_size():
     assert binding.bwd_workspace_bytes(1, 1, 128) == 4096 + 128 * 64 * 4
     assert binding.bwd_workspace_bytes(1, 1, 8, 32) == 0
     assert binding.bwd_workspace_bytes(0, 1, 8) == 0
+
+
+def test_window_arguments_rejected_on_host(lib):
+    def call(left=4, right=4, d=64, q=A, n_q=8):
+        return binding.attn_fwd_window_raw(q, A, A, A, None, 1, 1, n_q, 8, d, 0.125, left, right,
+                                           None)
+    assert call(left=-1) == binding.ATTN_ERR_INVALID_ARG
+    assert call(right=-5) == binding.ATTN_ERR_INVALID_ARG
+    assert call(q=None) == binding.ATTN_ERR_INVALID_ARG
+    assert call(n_q=0) == binding.ATTN_ERR_INVALID_ARG
+    assert call(d=32) == binding.ATTN_ERR_UNSUPPORTED

@@ -28,7 +28,7 @@ ATTN_ERR_SCRATCH_TOO_SMALL = -5
 DECODE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 # Every entry point declared in include/attn.h.
-EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_decode", "attn_decode_workspace_bytes",
+EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_fwd_window", "attn_decode", "attn_decode_workspace_bytes",
            "attn_decode_noalloc", "attn_bwd", "attn_bwd_workspace_bytes",
            "attn_check", "attn_status_string",
            "attn_last_cuda_error", "attn_set_wait_limit_ns", "attn_launch_count",
@@ -63,6 +63,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.restype = i32
             fn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, vp]
+        lib.attn_fwd_window.restype = i32
+        lib.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, i32,
+                                        vp]
         lib.attn_decode.restype = i32
         lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp,
                                     ctypes.c_size_t, vp]
@@ -157,6 +160,40 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | N
                       int(mask), _ptr(kl), _stream_ptr(stream), f32=q.dtype == torch.float32)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_window_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, n_k, d_k, scale, left,
+                       right, stream_ptr) -> int:
+    """The C call itself, on raw device pointers; returns the status code."""
+    return load().attn_fwd_window(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, n_k, d_k,
+                                  float(scale), int(left), int(right), stream_ptr)
+
+
+def attn_fwd_window(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, left: int, right: int,
+                    scale: float | None = None, out: torch.Tensor | None = None,
+                    lse: torch.Tensor | None = None, with_lse: bool = True, stream=None):
+    """Restricted self-attention on the GPU: query i sees keys i-left .. i+right.
+
+    q, k, v: contiguous bf16 CUDA [B, h, n, 64] tensors.  Returns (o, lse).
+    """
+    for t in (q, k, v):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 CUDA [B, h, n, d] tensors")
+    B, h, n_q, d = q.shape
+    n_k = k.shape[2]
+    if tuple(k.shape) != (B, h, n_k, d) or tuple(v.shape) != (B, h, n_k, d):
+        raise ValueError("k and v must be [B, h, n_k, d] with q's B, h, d")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty((B, h, n_q), dtype=torch.float32, device=q.device)
+    rc = attn_fwd_window_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, h, n_q, n_k, d,
+                             scale, left, right, _stream_ptr(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_window")
     return out, lse
 
 

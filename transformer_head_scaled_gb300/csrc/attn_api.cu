@@ -222,6 +222,32 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   return ATTN_OK;
 }
 
+int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+                    int n_q, int n_k, int d_k, float scale, int window_left, int window_right,
+                    struct CUstream_st* stream) {
+  int rc = check_common(q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, ATTN_MASK_NONE, nullptr, 2);
+  if (rc != ATTN_OK) return rc;
+  if (window_left < 0 || window_right < 0) return ATTN_ERR_INVALID_ARG;
+  if (d_k != 64) return ATTN_ERR_UNSUPPORTED;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di)) != ATTN_OK) return rc;
+  const long long bh = static_cast<long long>(B) * h;
+  CUtensorMap tmq, tmk, tmv, tmo;
+  if ((rc = encode_3d(&tmq, q, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&tmk, k, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&tmv, v, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(&tmo, o, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
+  // a side longer than both sequences changes nothing; clamping keeps the
+  // kernel's index arithmetic within int
+  const int reach = n_q + n_k;
+  Problem pb{q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, kMaskBand, nullptr,
+             window_left < reach ? window_left : reach, window_right < reach ? window_right : reach};
+  cudaError_t e = launch_fwd_tc(pb, tmq, tmk, tmv, tmo, make_ctx(*di, stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
 int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
                  int h, int n_q, int n_k, int d_k, float scale, int mask_kind,
                  const int* key_lens, struct CUstream_st* stream) {

@@ -6,7 +6,8 @@
 // What is computed is eq. (1) of "Attention Is All You Need" (section 3.2.1),
 // softmax(Q K^T / sqrt(d_k)) V per head, with the forbidden connections of
 // section 3.2.3 set to -inf before the softmax (causal: key j > query i;
-// key padding: key j >= key_lens[b]).  The streaming (online) softmax is an
+// key padding: key j >= key_lens[b]; restricted self-attention, section 4 and
+// Table 1: key j outside [i - left, i + right]).  The streaming (online) softmax is an
 // exact re-association of the row softmax: the pages name it only through
 // FlashAttention ("32 Transformer": exact attention without materialising
 // the N x N matrix).
@@ -89,6 +90,7 @@ struct Params {
   const int* key_lens;
   int H, n_q, n_k, BH;
   int mask;
+  int win_left, win_right;  // restricted self-attention window (band mask only)
   int num_qblocks;
   int num_items;
   float scale_log2;  // scale * log2(e): exp(scale*s) = 2^(s*scale_log2)
@@ -96,14 +98,17 @@ struct Params {
   int* status;
 };
 
-// A work item: 256 query rows of one (b, h).  n[s] = K/V tiles Q tile s
-// visits (0 when the tile lies past n_q).
+// A work item: 256 query rows of one (b, h).  Its K/V tiles are j0, j0+1,
+// ...; n[s] = how many of them Q tile s visits (0 when the tile lies past
+// n_q or sees no key).
 struct Item {
   int bh, qb;
   int key_limit;
+  int j0;
   int n[QT];
 };
 
+template <bool BAND>
 __device__ __forceinline__ Item decode_item(const Params& p, int t) {
   Item it;
   if (p.mask == kMaskCausal) {
@@ -122,6 +127,11 @@ __device__ __forceinline__ Item decode_item(const Params& p, int t) {
   }
   it.key_limit = limit;
   const int tiles = (limit + BN - 1) / BN;
+  it.j0 = 0;
+  if (BAND) {
+    // the first tile of the item's stream: the lowest key of its first row's window
+    it.j0 = max(it.qb * ROWS - p.win_left, 0) / BN;
+  }
 #pragma unroll
   for (int s = 0; s < QT; ++s) {
     const int row0 = it.qb * ROWS + s * BM;
@@ -131,6 +141,12 @@ __device__ __forceinline__ Item decode_item(const Params& p, int t) {
     } else if (p.mask == kMaskCausal) {
       const int last_row = min(row0 + BM - 1, p.n_q - 1);
       n = min(tiles, last_row / BN + 1);
+    } else if (BAND) {
+      // tiles j0 .. the one holding the highest key of this tile's last window
+      const int last_row = min(row0 + BM - 1, p.n_q - 1);
+      const int lo = max(row0 - p.win_left, 0);
+      const int hi = min(last_row + p.win_right, limit - 1);
+      n = lo > hi ? 0 : hi / BN - it.j0 + 1;
     }
     it.n[s] = n;
   }
@@ -142,6 +158,9 @@ __device__ __forceinline__ void record_timeout(const Params& p, Smem& sm) {
   *reinterpret_cast<volatile int*>(&sm.abort) = 1;
 }
 
+// BAND = restricted self-attention (its own instantiation, so that the
+// other masks' code is not touched by the window logic).
+template <bool BAND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk,
@@ -211,7 +230,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t items = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x, ++items) {
-        const Item it = decode_item(p, t);
+        const Item it = decode_item<BAND>(p, t);
         const int nmax = max(it.n[0], it.n[1]);
         // Q tiles of this item into buffer items % 2 (free once the S
         // products of item - 2 are done), then its K tiles.
@@ -232,7 +251,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = mbar_wait(smem_u32(&empty[slot]), ph ^ 1, p.limit_ns, abort);
           if (!ok) break;
           mbar_arrive_expect_tx(smem_u32(&full[slot]), TILE_BYTES);
-          tma_load_3d(smem_u32(ring + slot * TILE_BYTES), map, smem_u32(&full[slot]), 0, j * BN,
+          tma_load_3d(smem_u32(ring + slot * TILE_BYTES), map, smem_u32(&full[slot]), 0,
+                      ((BAND ? it.j0 : 0) + j) * BN,
                       it.bh);
           ++cnt;
         }
@@ -322,7 +342,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
       uint32_t g0 = 0, items = 0;
       for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x, ++items) {
-        const Item it = decode_item(p, t);
+        const Item it = decode_item<BAND>(p, t);
         const int n = it.n[s];
         const int nmax = max(it.n[0], it.n[1]);
         // The previous item's last PV product goes first unless this item's
@@ -386,6 +406,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tO = tmem + lane_off + col_o(s);
     const uint32_t tP = tmem + lane_off + col_p(s);
     const bool causal = p.mask == kMaskCausal;
+    constexpr bool band = BAND;
     const float c = p.scale_log2;
     uint32_t u = 0;  // tiles this stage has processed (all items)
     // Ping-pong: on the tiles both Q tiles visit, the two softmax warpgroups
@@ -396,7 +417,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (s == 1) mbar_arrive(smem_u32(&sm.turn[0]));  // Q tile 0 goes first
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
-      const Item it = decode_item(p, t);
+      const Item it = decode_item<BAND>(p, t);
       const int row0 = it.qb * ROWS + s * BM;
       const int row = row0 + quarter * 32 + lane;
       float m = -INFINITY;  // running max of scale*log2(e)*score (possibly stale)
@@ -419,15 +440,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.s_free[s]));
 
-        const int kbase = j * BN;
-        if (kbase + BN > it.key_limit || (causal && kbase + BN - 1 > row0)) {
+        const int kbase = ((BAND ? it.j0 : 0) + j) * BN;
+        if (kbase + BN > it.key_limit || (causal && kbase + BN - 1 > row0) ||
+            (band && (kbase < row0 + BM - 1 - p.win_left || kbase + BN - 1 > row0 + p.win_right))) {
           int lim = it.key_limit - kbase;  // columns >= lim are forbidden
+          int lo = 0;                      // and columns < lo
           if (causal) lim = min(lim, row - kbase + 1);
+          if (band) {
+            lim = min(lim, row + p.win_right - kbase + 1);
+            lo = row - p.win_left - kbase;
+          }
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (q4 * 32 + i >= lim) r[q4][i] = __float_as_uint(-INFINITY);
+              if (q4 * 32 + i >= lim || q4 * 32 + i < lo) r[q4][i] = __float_as_uint(-INFINITY);
         }
 
         float mx[4];
@@ -583,6 +610,8 @@ cudaError_t launch_fwd_tc(const Problem& pb, const CUtensorMap& tmq, const CUten
   p.n_k = pb.n_k;
   p.BH = pb.B * pb.H;
   p.mask = pb.mask;
+  p.win_left = pb.win_left;
+  p.win_right = pb.win_right;
   p.num_qblocks = (pb.n_q + ROWS - 1) / ROWS;
   p.num_items = p.BH * p.num_qblocks;
   p.scale_log2 = pb.scale * 1.4426950408889634f;
@@ -591,16 +620,21 @@ cudaError_t launch_fwd_tc(const Problem& pb, const CUtensorMap& tmq, const CUten
   const size_t smem = fwd_tc_smem_bytes();
   // The register hand-over inside the kernel assumes the launch holds
   // LAUNCH_REGS per thread; refuse to launch a build that does not.
+  const bool band = pb.mask == kMaskBand;
+  const void* fn = band ? reinterpret_cast<const void*>(attn_fwd_tc_kernel<true>)
+                        : reinterpret_cast<const void*>(attn_fwd_tc_kernel<false>);
   cudaFuncAttributes attr;
-  cudaError_t err = cudaFuncGetAttributes(&attr, attn_fwd_tc_kernel);
+  cudaError_t err = cudaFuncGetAttributes(&attr, fn);
   if (err != cudaSuccess) return err;
   if (attr.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-  err = cudaFuncSetAttribute(attn_fwd_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int grid = p.num_items < ctx.num_sms ? p.num_items : ctx.num_sms;
-  attn_fwd_tc_kernel<<<grid, NUM_THREADS, smem, ctx.stream>>>(tmq, tmk, tmv, tmo, p);
+  if (band)
+    attn_fwd_tc_kernel<true><<<grid, NUM_THREADS, smem, ctx.stream>>>(tmq, tmk, tmv, tmo, p);
+  else
+    attn_fwd_tc_kernel<false><<<grid, NUM_THREADS, smem, ctx.stream>>>(tmq, tmk, tmv, tmo, p);
   return cudaGetLastError();
 }
 

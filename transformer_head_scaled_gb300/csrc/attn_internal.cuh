@@ -8,7 +8,7 @@
 
 namespace attn {
 
-enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskKeyPadding = 2 };
+enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskKeyPadding = 2, kMaskBand = 3 };
 
 // Written (first error wins) into the library's device status word.
 enum DeviceStatus : int { kDevOk = 0, kDevTimeout = 1 };
@@ -24,6 +24,7 @@ struct Problem {
   float scale;
   int mask;
   const int* key_lens;
+  int win_left, win_right;  // kMaskBand: query i sees keys i - win_left .. i + win_right
 };
 
 // Launch context shared by every launcher.

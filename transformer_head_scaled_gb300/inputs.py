@@ -32,6 +32,7 @@ import torch
 MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_KEY_PADDING = 2
+MASK_BAND = 3  # restricted self-attention: query i sees keys i - win_left .. i + win_right
 
 SEED_Q, SEED_K, SEED_V, SEED_LENS, SEED_DOUT = 0, 1, 2, 3, 4
 
@@ -51,6 +52,8 @@ class Workload:
     lens_lo: int = 64
     kind: str = "fwd"  # "fwd": fused forward; "decode": few queries against a cache;
     #                    "bwd": gradients of the forward
+    win_left: int = 0   # MASK_BAND only
+    win_right: int = 0
     note: str = field(default="", compare=False)
 
     @property
@@ -85,6 +88,12 @@ WORKLOADS = {
     "decode_long": Workload("decode_long", 32, 16, 1, 4096, 64, MASK_KEY_PADDING, "bf16",
                             lens_lo=2048, kind="decode",
                             note="big model, 8 sentences x beam 4, cache up to 4096"),
+    # Restricted self-attention for long sequences ("Lire << Attention Is All
+    # You Need >>", section 4 and Table 1): a window of 2*256 + 1 positions
+    # centred on each output position of the big model's long sequences.
+    "big_window": Workload("big_window", 8, 16, 4096, 4096, 64, MASK_BAND, "bf16",
+                           win_left=256, win_right=256,
+                           note="big model, long sequence, window of 513 centred positions"),
     # Training needs the gradient of every attention layer (section 5 of
     # "Attention Is All You Need"): the backward on the same problems.
     "base_enc_bwd": Workload("base_enc_bwd", 64, 8, 512, 512, 64, MASK_NONE, "bf16", kind="bwd",
@@ -152,12 +161,27 @@ def flops(w: Workload, key_lens=None) -> float:
     f = 2.0 * products(w) * w.B * w.h * w.n_q * w.n_k * w.d
     if w.mask == MASK_CAUSAL:
         f *= 0.5
+    if w.mask == MASK_BAND:
+        # the work the window leaves: O(r n d) instead of O(n^2 d)
+        f = 2.0 * products(w) * w.B * w.h * band_pairs(w.n_q, w.n_k, w.win_left,
+                                                       w.win_right) * w.d
     return f
+
+
+def band_pairs(n_q: int, n_k: int, left: int, right: int) -> float:
+    """Number of (query, key) pairs inside the window i-left <= j <= i+right."""
+    i = np.arange(n_q, dtype=np.int64)
+    cnt = np.minimum(n_k - 1, i + right) - np.maximum(0, i - left) + 1
+    return float(np.maximum(cnt, 0).sum())
 
 
 def algorithmic_flops(w: Workload, key_lens=None) -> float:
     """FLOPs over the connections the mask allows: causal counts the exact
-    triangle, key padding counts sum_b L_b keys per query."""
+    triangle, key padding counts sum_b L_b keys per query, the band counts
+    the pairs inside each query's window."""
+    if w.mask == MASK_BAND:
+        return 2.0 * products(w) * w.B * w.h * band_pairs(w.n_q, w.n_k, w.win_left,
+                                                          w.win_right) * w.d
     if w.mask == MASK_CAUSAL:
         n = min(w.n_q, w.n_k)
         pairs = n * (n + 1) / 2 + max(0, w.n_q - n) * w.n_k
