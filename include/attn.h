@@ -63,7 +63,10 @@ typedef enum {
  *   q, k, v : const __nv_bfloat16*, layout above, 16-byte aligned.
  *   o       : __nv_bfloat16* [B,h,n_q,d_k], written (rounded to nearest even).
  *   lse     : float* [B,h,n_q] or NULL (then not written).
- *   B, h, n_q, n_k >= 1; d_k must be 64 (other head sizes: ATTN_ERR_UNSUPPORTED).
+ *   B, h, n_q, n_k >= 1; d_k in {16, 32, 64, 128} (the head sizes of the
+ *             model variants of "Attention Is All You Need", Table 3, rows (A)
+ *             and (B), that fit the tensor-core path; others:
+ *             ATTN_ERR_UNSUPPORTED).
  *   scale   : finite and > 0 (normally 1/sqrt(d_k)).
  *   mask_kind : an attn_mask_kind.
  *   key_lens  : device int32[B], required for ATTN_MASK_KEY_PADDING, ignored
@@ -87,7 +90,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  * long sequences (section 4 and Table 1: O(r n d) work instead of O(n^2 d));
  * window_right = 0 gives a causal window of window_left + 1 positions.
  * Tiles outside every row's window are never loaded.  Arguments otherwise as
- * attn_fwd (bf16, d_k = 64); window_left, window_right >= 0
+ * attn_fwd (bf16, d_k in {16, 32, 64, 128}); window_left, window_right >= 0
  * (ATTN_ERR_INVALID_ARG otherwise).  A query whose window holds no key
  * (i - window_left >= n_k) gets O = 0, LSE = -inf.
  */

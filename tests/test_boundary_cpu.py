@@ -81,7 +81,7 @@ def test_invalid_arguments_rejected_on_host(lib, f32):
 
 def test_unsupported_head_sizes(lib):
     UNS = binding.ATTN_ERR_UNSUPPORTED
-    for d in (16, 32, 48, 128):
+    for d in (8, 48, 96, 256):
         assert _call(False, d=d) == UNS
     for d in (8, 48, 96, 256):
         assert _call(True, d=d) == UNS
@@ -164,4 +164,4 @@ def test_window_arguments_rejected_on_host(lib):
     assert call(right=-5) == binding.ATTN_ERR_INVALID_ARG
     assert call(q=None) == binding.ATTN_ERR_INVALID_ARG
     assert call(n_q=0) == binding.ATTN_ERR_INVALID_ARG
-    assert call(d=32) == binding.ATTN_ERR_UNSUPPORTED
+    assert call(d=48) == binding.ATTN_ERR_UNSUPPORTED

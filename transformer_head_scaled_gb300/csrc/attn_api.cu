@@ -106,18 +106,23 @@ int check_common(const void* q, const void* k, const void* v, const void* o, con
   return ATTN_OK;
 }
 
-// (d, n, B*H) bf16 view with a (64, rows, 1) box and 128-byte swizzle.
+// (d, n, B*H) bf16 view with a (min(d, 64), rows, 1) box in the widest
+// swizzle its 2*min(d, 64)-byte rows fit: 128, 64 or 32 bytes (d = 128 is
+// copied as two 64-column boxes).
 int encode_3d(CUtensorMap* map, const void* base, int d, int n, long long bh, int box_rows) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
                         static_cast<cuuint64_t>(bh)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(n)};
-  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  const int inner = d < 64 ? d : 64;
+  const CUtensorMapSwizzle swz = inner == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : inner == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_32B;
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(inner), static_cast<cuuint32_t>(box_rows), 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
 }
 
@@ -133,6 +138,22 @@ int encode_3d_f32(CUtensorMap* map, const void* base, int n, long long bh) {
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
+}
+
+// Head sizes the tensor-core forward covers.
+bool tc_head_size(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+// The forward's four maps: Q and O with 128-row boxes, K and V with the key
+// tile of this head size.
+int encode_fwd_maps(CUtensorMap* tmq, CUtensorMap* tmk, CUtensorMap* tmv, CUtensorMap* tmo,
+                    const void* q, const void* k, const void* v, const void* o, int d, int n_q,
+                    int n_k, long long bh) {
+  const int kv_rows = fwd_tc_kv_rows(d);
+  int rc;
+  if ((rc = encode_3d(tmq, q, d, n_q, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(tmk, k, d, n_k, bh, kv_rows)) != ATTN_OK) return rc;
+  if ((rc = encode_3d(tmv, v, d, n_k, bh, kv_rows)) != ATTN_OK) return rc;
+  return encode_3d(tmo, o, d, n_q, bh, 128);
 }
 
 int encode_2d(CUtensorMap* map, const void* base) {
@@ -205,15 +226,13 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              struct CUstream_st* stream) {
   int rc = check_common(q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, mask_kind, key_lens, 2);
   if (rc != ATTN_OK) return rc;
-  if (d_k != 64) return ATTN_ERR_UNSUPPORTED;
+  if (!tc_head_size(d_k)) return ATTN_ERR_UNSUPPORTED;
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di)) != ATTN_OK) return rc;
   const long long bh = static_cast<long long>(B) * h;
   CUtensorMap tmq, tmk, tmv, tmo;
-  if ((rc = encode_3d(&tmq, q, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&tmk, k, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&tmv, v, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&tmo, o, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_fwd_maps(&tmq, &tmk, &tmv, &tmo, q, k, v, o, d_k, n_q, n_k, bh)) != ATTN_OK)
+    return rc;
   Problem pb{q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, mask_kind,
              mask_kind == ATTN_MASK_KEY_PADDING ? key_lens : nullptr};
   cudaError_t e = launch_fwd_tc(pb, tmq, tmk, tmv, tmo, make_ctx(*di, stream));
@@ -228,15 +247,13 @@ int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float*
   int rc = check_common(q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, ATTN_MASK_NONE, nullptr, 2);
   if (rc != ATTN_OK) return rc;
   if (window_left < 0 || window_right < 0) return ATTN_ERR_INVALID_ARG;
-  if (d_k != 64) return ATTN_ERR_UNSUPPORTED;
+  if (!tc_head_size(d_k)) return ATTN_ERR_UNSUPPORTED;
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di)) != ATTN_OK) return rc;
   const long long bh = static_cast<long long>(B) * h;
   CUtensorMap tmq, tmk, tmv, tmo;
-  if ((rc = encode_3d(&tmq, q, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&tmk, k, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&tmv, v, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&tmo, o, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_fwd_maps(&tmq, &tmk, &tmv, &tmo, q, k, v, o, d_k, n_q, n_k, bh)) != ATTN_OK)
+    return rc;
   // a side longer than both sequences changes nothing; clamping keeps the
   // kernel's index arithmetic within int
   const int reach = n_q + n_k;

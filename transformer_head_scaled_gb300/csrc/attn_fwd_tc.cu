@@ -40,12 +40,6 @@ using namespace ptx;
 constexpr int BM = 128;      // query rows per Q tile (= tensor-memory lanes)
 constexpr int QT = 2;        // Q tiles per work item
 constexpr int ROWS = BM * QT;
-constexpr int BN = 128;      // keys per K/V tile
-constexpr int D = 64;        // head size
-constexpr int QBUF = 2;      // Q tiles double-buffered: the next item's Q loads during this one
-constexpr int KSTAGES = 3;   // K ring depth
-constexpr int VSTAGES = 4;   // V ring depth (a V tile is held about two tiles longer than a K tile)
-constexpr uint32_t TILE_BYTES = BM * D * 2;  // a Q, K or V tile: 16 KB
 constexpr int LOAD_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int VLOAD_WARP = 10;
@@ -65,18 +59,50 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_THRESHOLD = 8.0f;
 constexpr float LN2 = 0.693147180559945309f;
 
-__host__ __device__ constexpr uint32_t col_s(int s) { return 128u * s; }
-__host__ __device__ constexpr uint32_t col_o(int s) { return 256u + 64u * s; }
-__host__ __device__ constexpr uint32_t col_p(int s) { return 384u + 64u * s; }
+// Tile shapes per head size d (16, 32, 64, 128; d_k = d_v).  A tile row of d
+// bf16 values is stored in 64-column blocks of RB bytes per row, each block
+// in the widest swizzle its row fits (128, 64 or 32 bytes), the layout a TMA
+// copy with that swizzle writes.  d = 128 takes 64-key K/V tiles so that S,
+// O and P of both Q tiles fit the 512 tensor-memory columns.
+template <int D_>
+struct Cfg {
+  static constexpr int D = D_;
+  static constexpr int BN = D_ == 128 ? 64 : 128;          // keys per K/V tile
+  static constexpr uint32_t RB = (D_ < 64 ? D_ : 64) * 2;  // bytes of a row in one block
+  static constexpr int NB = D_ > 64 ? D_ / 64 : 1;          // 64-column blocks per row
+  // shared-memory descriptor layout code: 2 = 128-byte, 4 = 64-byte, 6 = 32-byte swizzle
+  static constexpr uint32_t SWZ = RB == 128 ? 2u : (RB == 64 ? 4u : 6u);
+  static constexpr int KPB = RB / 32;                       // 16-element K steps per block row
+  static constexpr int QBUF = D_ == 128 ? 1 : 2;  // Q double-buffered: the next item's Q loads early
+  static constexpr int KSTAGES = 3;               // K ring depth
+  static constexpr int VSTAGES = D_ == 128 ? 3 : 4;  // V is held about two tiles longer than K
+  static constexpr uint32_t Q_TILE = BM * D_ * 2;    // a Q (or O) tile
+  static constexpr uint32_t KV_TILE = BN * D_ * 2;   // a K or V tile
+  static constexpr uint32_t Q_BLOCK = BM * RB;       // one column block of a Q tile
+  static constexpr uint32_t KV_BLOCK = BN * RB;
+  static constexpr uint32_t OW = D_ < 32 ? 32 : D_;  // tensor-memory columns per O accumulator
+  __host__ __device__ static constexpr uint32_t col_s(int s) { return BN * s; }
+  __host__ __device__ static constexpr uint32_t col_o(int s) { return 2 * BN + OW * s; }
+  __host__ __device__ static constexpr uint32_t col_p(int s) {
+    return 2 * BN + 2 * OW + (BN / 2) * s;
+  }
+  // the 16-byte chunk position XOR of row r inside its swizzle atom
+  __host__ __device__ static constexpr uint32_t swz(uint32_t r) {
+    return ((r * RB) >> 7) & (RB / 16 - 1);
+  }
+  static_assert(col_p(QT) <= 512, "tensor memory");
+};
 
+template <int D_>
 struct __align__(1024) Smem {
-  uint8_t q[QBUF][QT][TILE_BYTES];
-  uint8_t k[KSTAGES][TILE_BYTES];
-  uint8_t v[VSTAGES][TILE_BYTES];
-  uint8_t o[QT][TILE_BYTES];  // epilogue staging of O for the TMA store
-  uint64_t q_full[QBUF][QT], q_empty[QBUF][QT];
-  uint64_t k_full[KSTAGES], k_empty[KSTAGES];
-  uint64_t v_full[VSTAGES], v_empty[VSTAGES];
+  using C = Cfg<D_>;
+  uint8_t q[C::QBUF][QT][C::Q_TILE];
+  uint8_t k[C::KSTAGES][C::KV_TILE];
+  uint8_t v[C::VSTAGES][C::KV_TILE];
+  uint8_t o[QT][C::Q_TILE];  // epilogue staging of O for the TMA store
+  uint64_t q_full[C::QBUF][QT], q_empty[C::QBUF][QT];
+  uint64_t k_full[C::KSTAGES], k_empty[C::KSTAGES];
+  uint64_t v_full[C::VSTAGES], v_empty[C::VSTAGES];
   uint64_t s_full[QT], s_free[QT], p_full[QT], pv_done[QT];
   uint64_t drain[QT];
   uint64_t turn[QT];  // softmax ping-pong: Q tile s may run its exp phase
@@ -108,7 +134,7 @@ struct Item {
   int n[QT];
 };
 
-template <bool BAND>
+template <bool BAND, int BN>
 __device__ __forceinline__ Item decode_item(const Params& p, int t) {
   Item it;
   if (p.mask == kMaskCausal) {
@@ -153,22 +179,39 @@ __device__ __forceinline__ Item decode_item(const Params& p, int t) {
   return it;
 }
 
-__device__ __forceinline__ void record_timeout(const Params& p, Smem& sm) {
+// Shared-memory matrix descriptor (same fields as sdesc_sw128) with the
+// layout code `swz` at bits 61-63.
+__device__ __forceinline__ uint64_t sdesc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                          uint32_t swz) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= static_cast<uint64_t>(swz) << 61;
+  return d;
+}
+
+template <class SmemT>
+__device__ __forceinline__ void record_timeout(const Params& p, SmemT& sm) {
   atomicCAS(p.status, kDevOk, kDevTimeout);
   *reinterpret_cast<volatile int*>(&sm.abort) = 1;
 }
 
 // BAND = restricted self-attention (its own instantiation, so that the
 // other masks' code is not touched by the window logic).
-template <bool BAND>
+template <bool BAND, int D_>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv,
                        const __grid_constant__ CUtensorMap tmo, const Params p) {
+  using C = Cfg<D_>;
+  constexpr int D = C::D, BN = C::BN, QBUF = C::QBUF, KSTAGES = C::KSTAGES,
+                VSTAGES = C::VSTAGES;
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~static_cast<uintptr_t>(1023));
+  Smem<D_>& sm = *reinterpret_cast<Smem<D_>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const volatile int* abort = &sm.abort;
@@ -230,7 +273,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t items = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x, ++items) {
-        const Item it = decode_item<BAND>(p, t);
+        const Item it = decode_item<BAND, BN>(p, t);
         const int nmax = max(it.n[0], it.n[1]);
         // Q tiles of this item into buffer items % 2 (free once the S
         // products of item - 2 are done), then its K tiles.
@@ -240,8 +283,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!ok) break;
           const uint32_t bar = smem_u32(&sm.q_full[qb][s]);
           if (it.n[s] > 0) {
-            mbar_arrive_expect_tx(bar, TILE_BYTES);
-            tma_load_3d(smem_u32(sm.q[qb][s]), &tmq, bar, 0, it.qb * ROWS + s * BM, it.bh);
+            mbar_arrive_expect_tx(bar, C::Q_TILE);
+#pragma unroll
+            for (int cb = 0; cb < C::NB; ++cb)
+              tma_load_3d(smem_u32(sm.q[qb][s]) + cb * C::Q_BLOCK, &tmq, bar, 64 * cb,
+                          it.qb * ROWS + s * BM, it.bh);
           } else {
             mbar_arrive(bar);
           }
@@ -250,10 +296,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t slot = cnt % stages, ph = (cnt / stages) & 1;
           ok = mbar_wait(smem_u32(&empty[slot]), ph ^ 1, p.limit_ns, abort);
           if (!ok) break;
-          mbar_arrive_expect_tx(smem_u32(&full[slot]), TILE_BYTES);
-          tma_load_3d(smem_u32(ring + slot * TILE_BYTES), map, smem_u32(&full[slot]), 0,
-                      ((BAND ? it.j0 : 0) + j) * BN,
-                      it.bh);
+          mbar_arrive_expect_tx(smem_u32(&full[slot]), C::KV_TILE);
+#pragma unroll
+          for (int cb = 0; cb < C::NB; ++cb)
+            tma_load_3d(smem_u32(ring + slot * C::KV_TILE) + cb * C::KV_BLOCK, map,
+                        smem_u32(&full[slot]), 64 * cb, ((BAND ? it.j0 : 0) + j) * BN, it.bh);
           ++cnt;
         }
       }
@@ -291,19 +338,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int s = warp == MMA_WARP ? 0 : 1;
       constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false, false);  // Q, K both K-major
       constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, false, true);    // V is MN-major
-      constexpr uint32_t TILE16 = TILE_BYTES >> 4;  // a tile step in descriptor units
-      // K-major, 128B swizzle, 8-row groups 1024 B apart; a 16-element K step
-      // is 32 bytes inside the swizzle row (+2 in descriptor units).
-      const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0][s]), 16, 1024);
-      const uint64_t dq1 = sdesc_sw128(smem_u32(sm.q[1][s]), 16, 1024);
-      const uint64_t dk = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
-      // V is the MN-major B operand: 16 keys (one K step) are 16 rows of
-      // 128 B (+128 in descriptor units); 8-row groups 1024 B apart (SBO).
-      // N = 64 is a single 128-byte swizzle atom, so the MN-direction stride
-      // (LBO) is never applied; it is set to the same 1024 B so that no
-      // reading of the fields leaves the tile.
-      const uint64_t dv = sdesc_sw128(smem_u32(sm.v[0]), 1024, 1024);
-      const uint32_t t_s = tmem + col_s(s), t_o = tmem + col_o(s), t_p = tmem + col_p(s);
+      constexpr uint32_t KV16 = C::KV_TILE >> 4;           // a ring slot in descriptor units
+      constexpr uint32_t QBUF16 = (QT * C::Q_TILE) >> 4;   // between the Q buffers
+      // K-major Q and K: 8-row groups 8*RB bytes apart; a 16-element K step
+      // is 32 bytes inside a swizzled row (+2 in descriptor units), the next
+      // 64-column block (d = 128) one block further.
+      const uint64_t dq0 = sdesc(smem_u32(sm.q[0][s]), 16, 8 * C::RB, C::SWZ);
+      const uint64_t dk = sdesc(smem_u32(sm.k[0]), 16, 8 * C::RB, C::SWZ);
+      auto qstep = [](int kk) {
+        return static_cast<uint32_t>((kk / C::KPB) * (C::Q_BLOCK >> 4) + (kk % C::KPB) * 2);
+      };
+      auto kstep = [](int kk) {
+        return static_cast<uint32_t>((kk / C::KPB) * (C::KV_BLOCK >> 4) + (kk % C::KPB) * 2);
+      };
+      // V is the MN-major B operand: 16 keys (one K step) are 16 rows of RB
+      // bytes (+RB in descriptor units); 8-row groups 8*RB bytes apart (SBO);
+      // the 64-column blocks of d = 128 one block apart (LBO; with a single
+      // block it is never applied).
+      const uint64_t dv = sdesc(smem_u32(sm.v[0]), C::KV_BLOCK, 8 * C::RB, C::SWZ);
+      const uint32_t t_s = tmem + C::col_s(s), t_o = tmem + C::col_o(s),
+                     t_p = tmem + C::col_p(s);
 
       const bool leader = elect_one();
       bool ok = true;
@@ -327,11 +381,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       auto flush_pv = [&]() {
         if (!pending || !wait(&sm.p_full[s], npv & 1) || !v_wait(pg)) return;
         tc_fence_after();
-        const uint64_t b = dv + (pg % VSTAGES) * TILE16;
+        const uint64_t b = dv + (pg % VSTAGES) * KV16;
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(t_o, t_p + kk * 8, b + 128 * kk, IDESC_O, (pj > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(t_o, t_p + kk * 8, b + C::RB * kk, IDESC_O, (pj > 0 || kk > 0) ? 1u : 0u);
           tc_commit(smem_u32(&sm.pv_done[s]));
           tc_commit(smem_u32(&sm.v_empty[pg % VSTAGES]));
         }
@@ -342,13 +396,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
       uint32_t g0 = 0, items = 0;
       for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x, ++items) {
-        const Item it = decode_item<BAND>(p, t);
+        const Item it = decode_item<BAND, BN>(p, t);
         const int n = it.n[s];
         const int nmax = max(it.n[0], it.n[1]);
         // The previous item's last PV product goes first unless this item's
         // first S product is ready to go ahead of it.
         const uint32_t qb = items % QBUF, qph = (items / QBUF) & 1;
-        const uint64_t dq = qb == 0 ? dq0 : dq1;
+        const uint64_t dq = dq0 + qb * QBUF16;
         if (pending && !test(&sm.q_full[qb][s], qph)) flush_pv();
         if (!wait(&sm.q_full[qb][s], qph)) break;
         if (n == 0 && leader) tc_commit(smem_u32(&sm.q_empty[qb][s]));
@@ -358,11 +412,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!k_wait(g)) break;
           if (u > 0 && !wait(&sm.s_free[s], (u - 1) & 1)) break;
           tc_fence_after();
-          const uint64_t b = dk + (g % KSTAGES) * TILE16;
+          const uint64_t b = dk + (g % KSTAGES) * KV16;
           if (leader) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss(t_s, dq + 2 * kk, b + 2 * kk, IDESC_S, kk > 0 ? 1u : 0u);
+              mma_ss(t_s, dq + qstep(kk), b + kstep(kk), IDESC_S, kk > 0 ? 1u : 0u);
             tc_commit(smem_u32(&sm.s_full[s]));
             tc_commit(smem_u32(&sm.k_empty[g % KSTAGES]));
             if (j == n - 1) tc_commit(smem_u32(&sm.q_empty[qb][s]));  // Q tile s no longer read
@@ -402,9 +456,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int s = warp >> 2;
     const int quarter = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_off + col_s(s);
-    const uint32_t tO = tmem + lane_off + col_o(s);
-    const uint32_t tP = tmem + lane_off + col_p(s);
+    const uint32_t tS = tmem + lane_off + C::col_s(s);
+    const uint32_t tO = tmem + lane_off + C::col_o(s);
+    const uint32_t tP = tmem + lane_off + C::col_p(s);
+    constexpr int SC = BN / 32;        // 32-column chunks of S
+    constexpr int OC = C::OW / 32;     // 32-column chunks of O
     const bool causal = p.mask == kMaskCausal;
     constexpr bool band = BAND;
     const float c = p.scale_log2;
@@ -417,7 +473,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (s == 1) mbar_arrive(smem_u32(&sm.turn[0]));  // Q tile 0 goes first
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_items && ok; t += gridDim.x) {
-      const Item it = decode_item<BAND>(p, t);
+      const Item it = decode_item<BAND, BN>(p, t);
       const int row0 = it.qb * ROWS + s * BM;
       const int row = row0 + quarter * 32 + lane;
       float m = -INFINITY;  // running max of scale*log2(e)*score (possibly stale)
@@ -427,15 +483,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        uint32_t r[4][32];
-        tmem_ld32(tS + 0, r[0]);
-        tmem_ld32(tS + 32, r[1]);
-        tmem_ld32(tS + 64, r[2]);
-        tmem_ld32(tS + 96, r[3]);
+        uint32_t r[SC][32];
+#pragma unroll
+        for (int q4 = 0; q4 < SC; ++q4) tmem_ld32(tS + 32 * q4, r[q4]);
         tmem_ld_wait(r[0]);
-        reg_fence(r[1]);
-        reg_fence(r[2]);
-        reg_fence(r[3]);
+#pragma unroll
+        for (int q4 = 1; q4 < SC; ++q4) reg_fence(r[q4]);
         // S is in registers: the next S product may overwrite its columns.
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.s_free[s]));
@@ -451,7 +504,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             lo = row - p.win_left - kbase;
           }
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
+          for (int q4 = 0; q4 < SC; ++q4)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (q4 * 32 + i >= lim || q4 * 32 + i < lo) r[q4][i] = __float_as_uint(-INFINITY);
@@ -461,7 +514,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
+        for (int q4 = 0; q4 < SC; ++q4)
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             mx[0] = max3(mx[0], __uint_as_float(r[q4][i + 0]), __uint_as_float(r[q4][i + 1]));
@@ -488,9 +541,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         const float neg_m = (m == -INFINITY) ? 0.f : -m;
         float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
-        uint32_t pk[2][32];
+        uint32_t pk[SC / 2][32];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < SC; ++q4) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
             float x0, x1, x2, x3;
@@ -521,7 +574,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (__any_sync(0xffffffffu, rescale_o)) {
           const float a = rescale_o ? alpha : 1.f;
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
+          for (int h2 = 0; h2 < OC; ++h2) {
             uint32_t oc[32];
             tmem_ld32(tO + h2 * 32, oc);
             tmem_ld_wait(oc);
@@ -530,8 +583,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_st32(tO + h2 * 32, oc);
           }
         }
-        tmem_st32(tP, pk[0]);
-        tmem_st32(tP + 32, pk[1]);
+#pragma unroll
+        for (int c2 = 0; c2 < SC / 2; ++c2) tmem_st32(tP + 32 * c2, pk[c2]);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.p_full[s]));
@@ -539,33 +592,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
 
       // ---------------------------------------------------------- epilogue
-      uint32_t o0[32], o1[32];
+      uint32_t oreg[OC][32];
       if (it.n[s] > 0) {
         ok = mbar_wait(smem_u32(&sm.pv_done[s]), (u - 1) & 1, p.limit_ns, abort);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        tmem_ld32(tO, o0);
-        tmem_ld32(tO + 32, o1);
-        tmem_ld_wait(o0);
-        reg_fence(o1);
+#pragma unroll
+        for (int h2 = 0; h2 < OC; ++h2) tmem_ld32(tO + 32 * h2, oreg[h2]);
+        tmem_ld_wait(oreg[0]);
+#pragma unroll
+        for (int h2 = 1; h2 < OC; ++h2) reg_fence(oreg[h2]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o0[i] = o1[i] = 0u;
+        for (int h2 = 0; h2 < OC; ++h2)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) oreg[h2][i] = 0u;
       }
-      // O / l -> bf16 -> this tile's staging buffer in the 128-byte swizzled
-      // layout of the O tensor map -> one TMA store per 128-row tile (rows
-      // past n_q are clipped by the copy).
+      // O / l -> bf16 -> this tile's staging buffer in the swizzled layout of
+      // the O tensor map -> one TMA store per 64-column block of the 128-row
+      // tile (rows past n_q are clipped by the copy).
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int r_local = quarter * 32 + lane;
       const bool leader = quarter == 0 && lane == 0;
       if (leader) bulk_wait_read_all();  // the previous store has read the buffer
       named_bar_sync(1 + s, BM);
-      const uint32_t rbase = smem_u32(sm.o[s]) + r_local * 128;
+      const uint32_t rbase = smem_u32(sm.o[s]) + r_local * C::RB;
+      constexpr int CPB = C::RB / 16;  // 16-byte chunks per block row
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const uint32_t* src = g < 4 ? o0 + g * 8 : o1 + (g - 4) * 8;
-        st_shared_v4(rbase + ((g ^ (r_local & 7)) << 4),
+      for (int g = 0; g < D / 8; ++g) {
+        const uint32_t* src = oreg[g / 4] + (g % 4) * 8;
+        st_shared_v4(rbase + (g / CPB) * C::Q_BLOCK + (((g % CPB) ^ C::swz(r_local)) << 4),
                      pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv),
                      pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv),
                      pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv),
@@ -574,7 +631,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       fence_proxy_async_smem();
       named_bar_sync(1 + s, BM);
       if (leader && row0 < p.n_q) {
-        tma_store_3d(&tmo, smem_u32(sm.o[s]), 0, row0, it.bh);
+#pragma unroll
+        for (int cb = 0; cb < C::NB; ++cb)
+          tma_store_3d(&tmo, smem_u32(sm.o[s]) + cb * C::Q_BLOCK, 64 * cb, row0, it.bh);
         bulk_commit_group();
       }
       if (row < p.n_q && p.lse != nullptr)
@@ -595,9 +654,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+template <bool BAND, int D_>
+cudaError_t launch_instance(const Params& p, const CUtensorMap& tmq, const CUtensorMap& tmk,
+                            const CUtensorMap& tmv, const CUtensorMap& tmo, const LaunchCtx& ctx) {
+  static_assert(sizeof(Smem<D_>) + 1024 <= 232448, "dynamic shared memory per CTA");
+  const size_t smem = sizeof(Smem<D_>) + 1024;
+  // The register hand-over inside the kernel assumes the launch holds
+  // LAUNCH_REGS per thread; refuse to launch a build that does not.
+  cudaFuncAttributes attr;
+  cudaError_t err = cudaFuncGetAttributes(&attr, attn_fwd_tc_kernel<BAND, D_>);
+  if (err != cudaSuccess) return err;
+  if (attr.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+  err = cudaFuncSetAttribute(attn_fwd_tc_kernel<BAND, D_>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  const int grid = p.num_items < ctx.num_sms ? p.num_items : ctx.num_sms;
+  attn_fwd_tc_kernel<BAND, D_><<<grid, NUM_THREADS, smem, ctx.stream>>>(tmq, tmk, tmv, tmo, p);
+  return cudaGetLastError();
+}
+
+template <int D_>
+cudaError_t launch_d(const Params& p, bool band, const CUtensorMap& tmq, const CUtensorMap& tmk,
+                     const CUtensorMap& tmv, const CUtensorMap& tmo, const LaunchCtx& ctx) {
+  return band ? launch_instance<true, D_>(p, tmq, tmk, tmv, tmo, ctx)
+              : launch_instance<false, D_>(p, tmq, tmk, tmv, tmo, ctx);
+}
+
 }  // namespace
 
-size_t fwd_tc_smem_bytes() { return sizeof(Smem) + 1024; }
+int fwd_tc_kv_rows(int d) { return d == 128 ? Cfg<128>::BN : Cfg<64>::BN; }
 
 cudaError_t launch_fwd_tc(const Problem& pb, const CUtensorMap& tmq, const CUtensorMap& tmk,
                           const CUtensorMap& tmv, const CUtensorMap& tmo, const LaunchCtx& ctx) {
@@ -617,25 +702,14 @@ cudaError_t launch_fwd_tc(const Problem& pb, const CUtensorMap& tmq, const CUten
   p.scale_log2 = pb.scale * 1.4426950408889634f;
   p.limit_ns = ctx.limit_ns;
   p.status = ctx.status;
-  const size_t smem = fwd_tc_smem_bytes();
-  // The register hand-over inside the kernel assumes the launch holds
-  // LAUNCH_REGS per thread; refuse to launch a build that does not.
   const bool band = pb.mask == kMaskBand;
-  const void* fn = band ? reinterpret_cast<const void*>(attn_fwd_tc_kernel<true>)
-                        : reinterpret_cast<const void*>(attn_fwd_tc_kernel<false>);
-  cudaFuncAttributes attr;
-  cudaError_t err = cudaFuncGetAttributes(&attr, fn);
-  if (err != cudaSuccess) return err;
-  if (attr.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-  err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
-  const int grid = p.num_items < ctx.num_sms ? p.num_items : ctx.num_sms;
-  if (band)
-    attn_fwd_tc_kernel<true><<<grid, NUM_THREADS, smem, ctx.stream>>>(tmq, tmk, tmv, tmo, p);
-  else
-    attn_fwd_tc_kernel<false><<<grid, NUM_THREADS, smem, ctx.stream>>>(tmq, tmk, tmv, tmo, p);
-  return cudaGetLastError();
+  switch (pb.d) {
+    case 16: return launch_d<16>(p, band, tmq, tmk, tmv, tmo, ctx);
+    case 32: return launch_d<32>(p, band, tmq, tmk, tmv, tmo, ctx);
+    case 64: return launch_d<64>(p, band, tmq, tmk, tmv, tmo, ctx);
+    case 128: return launch_d<128>(p, band, tmq, tmk, tmv, tmo, ctx);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace attn

@@ -35,11 +35,13 @@ struct LaunchCtx {
   cudaStream_t stream;
 };
 
-// tcgen05 bf16 path (d = 64).  The tensor maps describe Q, K, V and O as
-// 3-D (d, n, B*H) bf16 tensors with a (64, 128, 1) box and 128-byte swizzle.
+// tcgen05 bf16 path, d in {16, 32, 64, 128}.  The tensor maps describe Q, K,
+// V and O as 3-D (d, n, B*H) bf16 tensors with a (min(d, 64), rows, 1) box
+// in the widest swizzle a box row fits (128, 64 or 32 bytes); rows = 128 for
+// Q and O, fwd_tc_kv_rows(d) for K and V.
 cudaError_t launch_fwd_tc(const Problem& pb, const CUtensorMap& tmq, const CUtensorMap& tmk,
                           const CUtensorMap& tmv, const CUtensorMap& tmo, const LaunchCtx& ctx);
-size_t fwd_tc_smem_bytes();
+int fwd_tc_kv_rows(int d);
 
 // fp32 SIMT path (d in {16, 32, 64, 128}).
 cudaError_t launch_fwd_f32(const Problem& pb, const LaunchCtx& ctx);

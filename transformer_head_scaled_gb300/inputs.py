@@ -88,6 +88,14 @@ WORKLOADS = {
     "decode_long": Workload("decode_long", 32, 16, 1, 4096, 64, MASK_KEY_PADDING, "bf16",
                             lens_lo=2048, kind="decode",
                             note="big model, 8 sentences x beam 4, cache up to 4096"),
+    # Other splits of the base model's d_model = 512 into heads ("Attention
+    # Is All You Need", Table 3, rows (A)): h x d_k = 4 x 128, 16 x 32, 32 x 16.
+    "base_h4_d128": Workload("base_h4_d128", 64, 4, 512, 512, 128, MASK_NONE, "bf16",
+                             note="base encoder self-attention, 4 heads of 128"),
+    "base_h16_d32": Workload("base_h16_d32", 64, 16, 512, 512, 32, MASK_NONE, "bf16",
+                             note="base encoder self-attention, 16 heads of 32"),
+    "base_h32_d16": Workload("base_h32_d16", 64, 32, 512, 512, 16, MASK_NONE, "bf16",
+                             note="base encoder self-attention, 32 heads of 16"),
     # Restricted self-attention for long sequences ("Lire << Attention Is All
     # You Need >>", section 4 and Table 1): a window of 2*256 + 1 positions
     # centred on each output position of the big model's long sequences.
