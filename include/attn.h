@@ -46,7 +46,8 @@ struct CUstream_st; /* cudaStream_t */
 typedef enum {
   ATTN_MASK_NONE = 0,
   ATTN_MASK_CAUSAL = 1,
-  ATTN_MASK_KEY_PADDING = 2
+  ATTN_MASK_KEY_PADDING = 2,
+  ATTN_MASK_WINDOW = 3 /* attn_fwd_strided only: the window of attn_fwd_window */
 } attn_mask_kind;
 
 typedef enum {
@@ -97,6 +98,24 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
                     int n_q, int n_k, int d_k, float scale, int window_left, int window_right,
                     struct CUstream_st* stream);
+
+/*
+ * attn_fwd_strided -- attn_fwd on tensors of any row, head and batch strides,
+ * e.g. [B, n, h, d] (the layout a projection to h heads produces) or Q, K, V
+ * packed in one [B, n, 3, h, d] buffer, without a copy.  Element (b, hh, i, t)
+ * of Q is  q[b*q_strides[0] + hh*q_strides[1] + i*q_strides[2] + t], and the
+ * same for k, v and o (o is written through its strides; lse stays
+ * contiguous [B, h, n_q]).  Strides are host arrays of 3 element counts, each
+ * > 0 and a multiple of 8 (16 bytes); d is contiguous.  mask_kind: any
+ * attn_mask_kind; ATTN_MASK_WINDOW uses window_left / window_right as
+ * attn_fwd_window does (both ignored otherwise).  bf16, d_k in {16, 32, 64,
+ * 128}; the tensors must not overlap o.  Other arguments as attn_fwd.
+ */
+int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int h, int n_q, int n_k, int d_k, const int64_t* q_strides,
+                     const int64_t* k_strides, const int64_t* v_strides, const int64_t* o_strides,
+                     float scale, int mask_kind, const int* key_lens, int window_left,
+                     int window_right, struct CUstream_st* stream);
 
 /*
  * attn_fwd_f32 -- float32 forward on the CUDA cores (fp32 FMA, same

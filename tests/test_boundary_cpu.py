@@ -165,3 +165,20 @@ def test_window_arguments_rejected_on_host(lib):
     assert call(q=None) == binding.ATTN_ERR_INVALID_ARG
     assert call(n_q=0) == binding.ATTN_ERR_INVALID_ARG
     assert call(d=48) == binding.ATTN_ERR_UNSUPPORTED
+
+
+def test_strided_arguments_rejected_on_host(lib):
+    good = [(8 * 64 * 8, 64, 8 * 64)] * 4   # [B, n, h, d] strides of a [B, h, n, d] view
+
+    def call(strides=good, mask=0, lens=None, left=0, right=0, d=64, q=A):
+        return binding.attn_fwd_strided_raw(q, A, A, A, None, 1, 8, 8, 8, d, strides, 0.125, mask,
+                                            lens, left, right, None)
+    INV = binding.ATTN_ERR_INVALID_ARG
+    assert call(strides=[(8 * 64 * 8, 64, 8 * 64 + 4)] + good[1:]) == INV  # not 16-byte strides
+    assert call(strides=good[:3] + [(0, 64, 512)]) == INV                   # zero stride
+    assert call(strides=good[:1] + [(-512, 64, 512)] + good[2:]) == INV     # negative stride
+    assert call(mask=3, left=-1) == INV
+    assert call(mask=4) == INV
+    assert call(mask=2, lens=None) == INV
+    assert call(q=None) == INV
+    assert call(d=48) == binding.ATTN_ERR_UNSUPPORTED

@@ -25,10 +25,11 @@ ATTN_ERR_UNSUPPORTED = -2
 ATTN_ERR_CUDA = -3
 ATTN_ERR_TIMEOUT = -4
 ATTN_ERR_SCRATCH_TOO_SMALL = -5
+MASK_WINDOW = 3  # attn_fwd_strided: the window of attn_fwd_window
 DECODE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 # Every entry point declared in include/attn.h.
-EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_fwd_window", "attn_decode", "attn_decode_workspace_bytes",
+EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_fwd_window", "attn_fwd_strided", "attn_decode", "attn_decode_workspace_bytes",
            "attn_decode_noalloc", "attn_bwd", "attn_bwd_workspace_bytes",
            "attn_check", "attn_status_string",
            "attn_last_cuda_error", "attn_set_wait_limit_ns", "attn_launch_count",
@@ -66,6 +67,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_fwd_window.restype = i32
         lib.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, i32,
                                         vp]
+        lib.attn_fwd_strided.restype = i32
+        lib.attn_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
+                                         vp, f32, i32, vp, i32, i32, vp]
         lib.attn_decode.restype = i32
         lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp,
                                     ctypes.c_size_t, vp]
@@ -194,6 +198,57 @@ def attn_fwd_window(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, left: int
                              scale, left, right, _stream_ptr(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_window")
+    return out, lse
+
+
+def attn_fwd_strided_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, n_k, d_k, strides, scale,
+                        mask_kind, lens_ptr, left, right, stream_ptr) -> int:
+    """The C call itself; ``strides`` = four (b, h, n) element-stride triples for q, k, v, o."""
+    arrs = [(ctypes.c_int64 * 3)(*[int(x) for x in st]) for st in strides]
+    return load().attn_fwd_strided(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, n_k, d_k,
+                                   *[ctypes.cast(a, ctypes.c_void_p) for a in arrs],
+                                   float(scale), int(mask_kind), lens_ptr, int(left), int(right),
+                                   stream_ptr)
+
+
+def attn_fwd_strided(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+                     mask: int = MASK_NONE, key_lens: torch.Tensor | None = None,
+                     window: tuple[int, int] | None = None, out: torch.Tensor | None = None,
+                     lse: torch.Tensor | None = None, with_lse: bool = True, stream=None):
+    """attn_fwd on [B, h, n, d] bf16 views with any strides over the first three
+    dimensions and a contiguous last one (e.g. ``x.view(B, n, h, d).transpose(1, 2)``).
+    ``window=(left, right)`` selects restricted self-attention; ``out`` may be a
+    strided view too (default: contiguous)."""
+    for t in (q, k, v):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or t.stride(-1) != 1:
+            raise ValueError("q, k, v must be bf16 CUDA [B, h, n, d] views with unit last stride")
+    B, h, n_q, d = q.shape
+    n_k = k.shape[2]
+    if tuple(k.shape) != (B, h, n_k, d) or tuple(v.shape) != (B, h, n_k, d):
+        raise ValueError("k and v must be [B, h, n_k, d] with q's B, h, d")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    kl, left, right = None, 0, 0
+    if window is not None:
+        mask, (left, right) = MASK_WINDOW, window
+    if mask == MASK_KEY_PADDING:
+        if key_lens is None:
+            raise ValueError("key padding needs key_lens")
+        kl = key_lens
+        if kl.dtype != torch.int32 or not kl.is_cuda or kl.numel() != B or not kl.is_contiguous():
+            raise ValueError("key_lens must be a contiguous int32 CUDA tensor of B entries")
+    if out is None:
+        out = torch.empty((B, h, n_q, d), dtype=q.dtype, device=q.device)
+    if tuple(out.shape) != (B, h, n_q, d) or out.stride(-1) != 1:
+        raise ValueError("out must be a [B, h, n_q, d] view with unit last stride")
+    if lse is None and with_lse:
+        lse = torch.empty((B, h, n_q), dtype=torch.float32, device=q.device)
+    strides = [t.stride()[:3] for t in (q, k, v, out)]
+    rc = attn_fwd_strided_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, h, n_q, n_k, d,
+                              strides, scale, int(mask), _ptr(kl), left, right,
+                              _stream_ptr(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_strided")
     return out, lse
 
 

@@ -143,17 +143,54 @@ int encode_3d_f32(CUtensorMap* map, const void* base, int n, long long bh) {
 // Head sizes the tensor-core forward covers.
 bool tc_head_size(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
+// Element strides of a [B, h, n, d] tensor view (d contiguous).
+struct Strides {
+  long long b, h, n;
+};
+
+Strides bhsd(int h, int n, int d) {
+  return Strides{static_cast<long long>(h) * n * d, static_cast<long long>(n) * d, d};
+}
+
+// A stride the TMA can use: positive and a multiple of 16 bytes.
+bool stride_ok(long long elems) {
+  return elems > 0 && (elems * 2) % 16 == 0 && elems * 2 < (1LL << 40);
+}
+
+// (d, n, h, B) bf16 view with the given strides and a (min(d, 64), rows, 1, 1)
+// box in the widest swizzle its 2*min(d, 64)-byte rows fit.
+int encode_4d(CUtensorMap* map, const void* base, int d, int n, int h, int B, Strides st,
+              int box_rows) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
+                        static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * 2, static_cast<cuuint64_t>(st.h) * 2,
+                           static_cast<cuuint64_t>(st.b) * 2};
+  const int inner = d < 64 ? d : 64;
+  const CUtensorMapSwizzle swz = inner == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : inner == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_32B;
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(inner), static_cast<cuuint32_t>(box_rows), 1u, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+
 // The forward's four maps: Q and O with 128-row boxes, K and V with the key
-// tile of this head size.
+// tile of this head size.  st = strides of q, k, v, o, or null for
+// contiguous [B, h, n, d].
 int encode_fwd_maps(CUtensorMap* tmq, CUtensorMap* tmk, CUtensorMap* tmv, CUtensorMap* tmo,
                     const void* q, const void* k, const void* v, const void* o, int d, int n_q,
-                    int n_k, long long bh) {
+                    int n_k, int h, int B, const Strides* st) {
   const int kv_rows = fwd_tc_kv_rows(d);
+  const Strides sq = st ? st[0] : bhsd(h, n_q, d), sk = st ? st[1] : bhsd(h, n_k, d),
+                sv = st ? st[2] : bhsd(h, n_k, d), so = st ? st[3] : bhsd(h, n_q, d);
   int rc;
-  if ((rc = encode_3d(tmq, q, d, n_q, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(tmk, k, d, n_k, bh, kv_rows)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(tmv, v, d, n_k, bh, kv_rows)) != ATTN_OK) return rc;
-  return encode_3d(tmo, o, d, n_q, bh, 128);
+  if ((rc = encode_4d(tmq, q, d, n_q, h, B, sq, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_4d(tmk, k, d, n_k, h, B, sk, kv_rows)) != ATTN_OK) return rc;
+  if ((rc = encode_4d(tmv, v, d, n_k, h, B, sv, kv_rows)) != ATTN_OK) return rc;
+  return encode_4d(tmo, o, d, n_q, h, B, so, 128);
 }
 
 int encode_2d(CUtensorMap* map, const void* base) {
@@ -229,9 +266,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (!tc_head_size(d_k)) return ATTN_ERR_UNSUPPORTED;
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di)) != ATTN_OK) return rc;
-  const long long bh = static_cast<long long>(B) * h;
   CUtensorMap tmq, tmk, tmv, tmo;
-  if ((rc = encode_fwd_maps(&tmq, &tmk, &tmv, &tmo, q, k, v, o, d_k, n_q, n_k, bh)) != ATTN_OK)
+  if ((rc = encode_fwd_maps(&tmq, &tmk, &tmv, &tmo, q, k, v, o, d_k, n_q, n_k, h, B, nullptr)) !=
+      ATTN_OK)
     return rc;
   Problem pb{q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, mask_kind,
              mask_kind == ATTN_MASK_KEY_PADDING ? key_lens : nullptr};
@@ -250,14 +287,58 @@ int attn_fwd_window(const void* q, const void* k, const void* v, void* o, float*
   if (!tc_head_size(d_k)) return ATTN_ERR_UNSUPPORTED;
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di)) != ATTN_OK) return rc;
-  const long long bh = static_cast<long long>(B) * h;
   CUtensorMap tmq, tmk, tmv, tmo;
-  if ((rc = encode_fwd_maps(&tmq, &tmk, &tmv, &tmo, q, k, v, o, d_k, n_q, n_k, bh)) != ATTN_OK)
+  if ((rc = encode_fwd_maps(&tmq, &tmk, &tmv, &tmo, q, k, v, o, d_k, n_q, n_k, h, B, nullptr)) !=
+      ATTN_OK)
     return rc;
   // a side longer than both sequences changes nothing; clamping keeps the
   // kernel's index arithmetic within int
   const int reach = n_q + n_k;
   Problem pb{q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, kMaskBand, nullptr,
+             window_left < reach ? window_left : reach, window_right < reach ? window_right : reach};
+  cudaError_t e = launch_fwd_tc(pb, tmq, tmk, tmv, tmo, make_ctx(*di, stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
+int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int h, int n_q, int n_k, int d_k, const int64_t* q_strides,
+                     const int64_t* k_strides, const int64_t* v_strides, const int64_t* o_strides,
+                     float scale, int mask_kind, const int* key_lens, int window_left,
+                     int window_right, struct CUstream_st* stream) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || h < 1 || n_q < 1 || n_k < 1 || d_k < 1) return ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_WINDOW) return ATTN_ERR_INVALID_ARG;
+  if (mask_kind == ATTN_MASK_KEY_PADDING &&
+      (key_lens == nullptr || (reinterpret_cast<uintptr_t>(key_lens) & 3u)))
+    return ATTN_ERR_INVALID_ARG;
+  if (mask_kind == ATTN_MASK_WINDOW && (window_left < 0 || window_right < 0))
+    return ATTN_ERR_INVALID_ARG;
+  if (!q_strides || !k_strides || !v_strides || !o_strides) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * h > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  Strides st[4];
+  const int64_t* in[4] = {q_strides, k_strides, v_strides, o_strides};
+  for (int i = 0; i < 4; ++i) {
+    st[i] = Strides{in[i][0], in[i][1], in[i][2]};
+    if (!stride_ok(st[i].b) || !stride_ok(st[i].h) || !stride_ok(st[i].n))
+      return ATTN_ERR_INVALID_ARG;
+  }
+  if (!tc_head_size(d_k)) return ATTN_ERR_UNSUPPORTED;
+  DeviceInfo* di = nullptr;
+  int rc;
+  if ((rc = device_info(&di)) != ATTN_OK) return rc;
+  CUtensorMap tmq, tmk, tmv, tmo;
+  if ((rc = encode_fwd_maps(&tmq, &tmk, &tmv, &tmo, q, k, v, o, d_k, n_q, n_k, h, B, st)) !=
+      ATTN_OK)
+    return rc;
+  const int reach = n_q + n_k;
+  Problem pb{q, k, v, o, lse, B, h, n_q, n_k, d_k, scale,
+             mask_kind == ATTN_MASK_WINDOW ? static_cast<int>(kMaskBand) : mask_kind,
+             mask_kind == ATTN_MASK_KEY_PADDING ? key_lens : nullptr,
              window_left < reach ? window_left : reach, window_right < reach ? window_right : reach};
   cudaError_t e = launch_fwd_tc(pb, tmq, tmk, tmv, tmo, make_ctx(*di, stream));
   if (e != cudaSuccess) return cuda_fail(e);

@@ -179,6 +179,26 @@ __device__ __forceinline__ Item decode_item(const Params& p, int t) {
   return it;
 }
 
+// 4-D tiled copies (coordinates: column, row, head, batch entry), so that the
+// caller's tensors may have any strides across rows, heads and batch entries.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int x, int y,
+                                             int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor (same fields as sdesc_sw128) with the
 // layout code `swz` at bits 61-63.
 __device__ __forceinline__ uint64_t sdesc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
@@ -286,8 +306,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive_expect_tx(bar, C::Q_TILE);
 #pragma unroll
             for (int cb = 0; cb < C::NB; ++cb)
-              tma_load_3d(smem_u32(sm.q[qb][s]) + cb * C::Q_BLOCK, &tmq, bar, 64 * cb,
-                          it.qb * ROWS + s * BM, it.bh);
+              tma_load_4d(smem_u32(sm.q[qb][s]) + cb * C::Q_BLOCK, &tmq, bar, 64 * cb,
+                          it.qb * ROWS + s * BM, it.bh % p.H, it.bh / p.H);
           } else {
             mbar_arrive(bar);
           }
@@ -299,8 +319,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_expect_tx(smem_u32(&full[slot]), C::KV_TILE);
 #pragma unroll
           for (int cb = 0; cb < C::NB; ++cb)
-            tma_load_3d(smem_u32(ring + slot * C::KV_TILE) + cb * C::KV_BLOCK, map,
-                        smem_u32(&full[slot]), 64 * cb, ((BAND ? it.j0 : 0) + j) * BN, it.bh);
+            tma_load_4d(smem_u32(ring + slot * C::KV_TILE) + cb * C::KV_BLOCK, map,
+                        smem_u32(&full[slot]), 64 * cb, ((BAND ? it.j0 : 0) + j) * BN,
+                        it.bh % p.H, it.bh / p.H);
           ++cnt;
         }
       }
@@ -633,7 +654,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (leader && row0 < p.n_q) {
 #pragma unroll
         for (int cb = 0; cb < C::NB; ++cb)
-          tma_store_3d(&tmo, smem_u32(sm.o[s]) + cb * C::Q_BLOCK, 64 * cb, row0, it.bh);
+          tma_store_4d(&tmo, smem_u32(sm.o[s]) + cb * C::Q_BLOCK, 64 * cb, row0, it.bh % p.H,
+                       it.bh / p.H);
         bulk_commit_group();
       }
       if (row < p.n_q && p.lse != nullptr)
