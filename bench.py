@@ -299,11 +299,13 @@ def run_reference(args, w):
     value = statistics.median(vals)
     cores = cpu_cores_used()
     if bwd:
-        desc = (f"{per_step_units} whole heads per step, drawn from the {w.B * w.h} heads of the "
-                f"workload (dQ, dK, dV of each), float64")
+        total = w.B * w.h
+        desc = (f"{per_step_units} whole heads per step ({per_step_units / total:.2f} passes over "
+                f"the {total} heads of the workload; dQ, dK, dV of each), float64")
     else:
-        desc = (f"{per_step_units} query rows per step, drawn from the {w.B * w.h * w.n_q} rows "
-                f"of the workload (each against all its visible keys), float64")
+        total = w.B * w.h * w.n_q
+        desc = (f"{per_step_units} query rows per step ({per_step_units / total:.2f} passes over "
+                f"the {total} rows of the workload, each against all its visible keys), float64")
     line = {
         "impl": "reference", "metric": metric_name(w), "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
