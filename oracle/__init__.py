@@ -76,6 +76,10 @@ def _load():
             bd.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_long] * 6 + [
                 ctypes.c_double, ctypes.c_long, ctypes.c_long, ctypes.c_void_p, ctypes.c_long,
                 ctypes.c_int]
+            hb = lib.oracle_attn_bwd_band_f64
+            hb.restype = ctypes.c_int
+            hb.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_long] * 6 + [
+                ctypes.c_double, ctypes.c_long, ctypes.c_long, ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -197,3 +201,22 @@ def attn_band(q, k, v, scale: float, left: int, right: int, rows=None, threads: 
     if rc != 0:
         raise RuntimeError(f"oracle_attn_band_f64 failed ({rc})")
     return o, lse
+
+
+def attn_bwd_band(q, k, v, dout, scale: float, left: int, right: int, threads: int = 0):
+    """Gradients (dq, dk, dv), float64, of restricted self-attention (attn_band)."""
+    q, k, v, _, (B, H, n_q, n_k, d_k, d_v) = _prep(q, k, v, MASK_NONE, None)
+    if left < 0 or right < 0:
+        raise ValueError("window sides must be >= 0")
+    g = _as_f32(dout)
+    if g.shape != (B, H, n_q, d_v):
+        raise ValueError("dout must be [B,H,n_q,d_v]")
+    dq = np.empty((B, H, n_q, d_k), dtype=np.float64)
+    dk = np.empty((B, H, n_k, d_k), dtype=np.float64)
+    dv = np.empty((B, H, n_k, d_v), dtype=np.float64)
+    rc = _load().oracle_attn_bwd_band_f64(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(dq), _ptr(dk), _ptr(dv), B, H, n_q, n_k,
+        d_k, d_v, float(scale), int(left), int(right), int(threads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_bwd_band_f64 failed ({rc})")
+    return dq, dk, dv

@@ -49,6 +49,7 @@
 #define ORACLE_MASK_NONE 0
 #define ORACLE_MASK_CAUSAL 1
 #define ORACLE_MASK_KEY_PADDING 2
+#define ORACLE_MASK_BAND 3 /* query i sees keys i - left .. i + right (restricted attention) */
 
 /* One query row: scores, mask, softmax, weighted sum.  `s` is n_k doubles of
  * scratch owned by the calling thread. */
@@ -210,11 +211,16 @@ int oracle_max_threads(void) {
  * layout as the forward, dO [B,H,n_q,d_v], dq/dk/dv like q/k/v.
  * Returns 0, -1 on bad arguments, -2 when scratch cannot be allocated.
  */
-int oracle_attn_bwd_f64(const float* q, const float* k, const float* v, const float* dout,
-                        double* dq, double* dk, double* dv, long B, long H, long n_q,
-                        long n_k, long d_k, long d_v, double scale, int mask_kind,
-                        const int* key_lens, int n_threads) {
-  if (oracle_check(B, H, n_q, n_k, d_k, d_v, mask_kind, key_lens)) return -1;
+static int bwd_core(const float* q, const float* k, const float* v, const float* dout,
+                    double* dq, double* dk, double* dv, long B, long H, long n_q, long n_k,
+                    long d_k, long d_v, double scale, int mask_kind, const int* key_lens,
+                    long left, long right, int n_threads) {
+  if (mask_kind == ORACLE_MASK_BAND) {
+    if (B < 0 || H < 0 || n_q < 0 || n_k < 0 || d_k < 1 || d_v < 1 || left < 0 || right < 0)
+      return -1;
+  } else if (oracle_check(B, H, n_q, n_k, d_k, d_v, mask_kind, key_lens)) {
+    return -1;
+  }
   int failed = 0;
 #ifdef _OPENMP
   if (n_threads > 0) omp_set_num_threads(n_threads);
@@ -250,7 +256,8 @@ int oracle_attn_bwd_f64(const float* q, const float* k, const float* v, const fl
     for (long i = 0; i < n_q; ++i) {
       double m = -INFINITY;
       for (long j = 0; j < n_k; ++j) {
-        int forbidden = (j >= limit) || (mask_kind == ORACLE_MASK_CAUSAL && j > i);
+        int forbidden = (j >= limit) || (mask_kind == ORACLE_MASK_CAUSAL && j > i) ||
+                        (mask_kind == ORACLE_MASK_BAND && (j < i - left || j > i + right));
         double s = -INFINITY;
         if (!forbidden) {
           double dot = 0.0;
@@ -388,4 +395,24 @@ int oracle_attn_band_f64(const float* q, const float* k, const float* v, double*
   }
   (void)n_threads;
   return failed ? -2 : 0;
+}
+
+/* The backward of the forward above (masks none, causal, key padding). */
+int oracle_attn_bwd_f64(const float* q, const float* k, const float* v, const float* dout,
+                        double* dq, double* dk, double* dv, long B, long H, long n_q,
+                        long n_k, long d_k, long d_v, double scale, int mask_kind,
+                        const int* key_lens, int n_threads) {
+  if (mask_kind == ORACLE_MASK_BAND) return -1;
+  return bwd_core(q, k, v, dout, dq, dk, dv, B, H, n_q, n_k, d_k, d_v, scale, mask_kind,
+                  key_lens, 0, 0, n_threads);
+}
+
+/* The backward of restricted self-attention (oracle_attn_band_f64): the same
+ * gradient with the window i - left <= j <= i + right as the mask. */
+int oracle_attn_bwd_band_f64(const float* q, const float* k, const float* v, const float* dout,
+                             double* dq, double* dk, double* dv, long B, long H, long n_q,
+                             long n_k, long d_k, long d_v, double scale, long left, long right,
+                             int n_threads) {
+  return bwd_core(q, k, v, dout, dq, dk, dv, B, H, n_q, n_k, d_k, d_v, scale, ORACLE_MASK_BAND,
+                  NULL, left, right, n_threads);
 }

@@ -231,3 +231,79 @@ def test_bad_arguments():
         oracle.attn_bwd(q, k, v, g[:, :, :2], 0.5)
     with pytest.raises(ValueError):
         oracle.attn_bwd(q, k, v, g, 0.5, oracle.MASK_KEY_PADDING, None)
+
+
+# ---------------------------------------------------------------- restricted window
+
+def _torch_band_grads(q, k, v, g, scale, left, right):
+    Q, K, V = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+    i = torch.arange(q.shape[2])[:, None]
+    j = torch.arange(k.shape[2])[None, :]
+    allowed = ((j >= i - left) & (j <= i + right))[None, None]
+    any_row = allowed.any(-1, keepdim=True)
+    s = scale * Q @ K.transpose(-1, -2)
+    s = torch.where(allowed, s, torch.tensor(-math.inf, dtype=torch.float64))
+    s = torch.where(any_row, s, torch.zeros((), dtype=torch.float64))
+    p = torch.softmax(s, dim=-1) * any_row
+    (p @ V * torch.tensor(g, dtype=torch.float64)).sum().backward()
+    return Q.grad.numpy(), K.grad.numpy(), V.grad.numpy()
+
+
+@pytest.mark.parametrize("left,right", [(2, 2), (4, 0), (0, 3), (1, 6), (0, 0)])
+def test_band_matches_autograd(left, right):
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((2, 2, 11, 5)).astype(np.float32)
+    k = rng.standard_normal((2, 2, 9, 5)).astype(np.float32)   # queries 9, 10 see few or no keys
+    v = rng.standard_normal((2, 2, 9, 4)).astype(np.float32)
+    g = rng.standard_normal((2, 2, 11, 4)).astype(np.float32)
+    got = oracle.attn_bwd_band(q, k, v, g, 0.45, left, right)
+    want = _torch_band_grads(q, k, v, g, 0.45, left, right)
+    for a, b in zip(got, want):
+        np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-12)
+
+
+def test_band_finite_differences_of_the_band_forward():
+    q, k, v, g = _inputs(n_q=6, n_k=7)
+    left, right = 2, 1
+    grads = oracle.attn_bwd_band(q, k, v, g, 0.5, left, right)
+    rng = np.random.default_rng(8)
+    for name, x, grad in zip(("q", "k", "v"), (q, k, v), grads):
+        for _ in range(5):
+            idx = tuple(int(rng.integers(0, n)) for n in x.shape)
+
+            def loss(h):
+                xs = {"q": q, "k": k, "v": v}
+                y = x.copy()
+                y[idx] += h
+                xs[name] = y
+                o, _ = oracle.attn_band(xs["q"], xs["k"], xs["v"], 0.5, left, right)
+                return float((o * g.astype(np.float64)).sum())
+
+            def central(h):
+                return (loss(h) - loss(-h)) / (2 * h)
+
+            h = 2.0 ** -9
+            est = (4 * central(h / 2) - central(h)) / 3
+            assert abs(est - grad[idx]) <= 1e-7 + 1e-6 * abs(grad[idx]), (name, idx)
+
+
+def test_band_limits_are_the_unmasked_and_causal_backward():
+    q, k, v, g = _inputs(n_q=6, n_k=6)
+    a = oracle.attn_bwd_band(q, k, v, g, 0.5, 100, 100)
+    b = oracle.attn_bwd(q, k, v, g, 0.5)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+    a = oracle.attn_bwd_band(q, k, v, g, 0.5, 100, 0)
+    b = oracle.attn_bwd(q, k, v, g, 0.5, oracle.MASK_CAUSAL)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_band_keys_outside_every_window_get_no_gradient():
+    q, k, v, g = _inputs(n_q=5, n_k=12)
+    dq, dk, dv = oracle.attn_bwd_band(q, k, v, g, 0.5, 1, 2)   # queries 0..4 reach keys <= 6
+    assert np.all(dk[:, :, 7:] == 0) and np.all(dv[:, :, 7:] == 0)
+    k2 = k.copy()
+    k2[:, :, 7:] = 9.0
+    again = oracle.attn_bwd_band(q, k2, v, g, 0.5, 1, 2)
+    np.testing.assert_array_equal(again[0], dq)
