@@ -244,7 +244,11 @@ def oracle_bwd_sample(w: inputs.Workload, q, k, v, g, kl, target_s: float, threa
         sub = lambda t: np.ascontiguousarray(t[b_idx, h_idx][:, None])  # noqa: E731
         sl = None if lens is None else lens[b_idx]
         t0 = time.perf_counter()
-        oracle.attn_bwd(sub(q), sub(k), sub(v), sub(g), w.scale, w.mask, sl, threads=threads)
+        if w.mask == inputs.MASK_BAND:
+            oracle.attn_bwd_band(sub(q), sub(k), sub(v), sub(g), w.scale, w.win_left,
+                                 w.win_right, threads=threads)
+        else:
+            oracle.attn_bwd(sub(q), sub(k), sub(v), sub(g), w.scale, w.mask, sl, threads=threads)
         dt = time.perf_counter() - t0
         rows = np.concatenate([np.arange(w.n_q) + int(bh) * w.n_q for bh in sel])
         return dt, _row_flops(w, rows, lens) * inputs.products(w) / 2.0
@@ -366,7 +370,11 @@ def run_ours(args, w):
     if bwd:
         # O and LSE of the same inputs come from the forward, outside the timing
         g = inputs.make_dout(w, device=dev, seed=inputs.SEED_DOUT + 8 * rank)
-        binding.attn_fwd(q, k, v, scale=w.scale, mask=w.mask, key_lens=kl, out=o, lse=lse)
+        if w.mask == inputs.MASK_BAND:
+            binding.attn_fwd_window(q, k, v, w.win_left, w.win_right, scale=w.scale, out=o,
+                                    lse=lse)
+        else:
+            binding.attn_fwd(q, k, v, scale=w.scale, mask=w.mask, key_lens=kl, out=o, lse=lse)
         grads = [torch.empty_like(t) for t in (q, k, v)]
         bptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), g.data_ptr(),
                  lse.data_ptr(), *(t.data_ptr() for t in grads))
@@ -375,6 +383,10 @@ def run_ours(args, w):
         if decode:
             rc = binding.attn_decode_raw(*ptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale, klp,
                                          ws.data_ptr(), ws_bytes, sptr)
+        elif bwd and w.mask == inputs.MASK_BAND:
+            rc = binding.attn_bwd_window_raw(*bptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale,
+                                             w.win_left, w.win_right, ws.data_ptr(), ws_bytes,
+                                             sptr)
         elif bwd:
             rc = binding.attn_bwd_raw(*bptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale, w.mask, klp,
                                       ws.data_ptr(), ws_bytes, sptr)
@@ -562,11 +574,19 @@ def run_e2e_bwd(args, w, q, k, v, o, lse, g, kl, dev, stream):
         if dkl is not None:
             dkl.copy_(hkl, non_blocking=True)
         qd, kd, vd, od, ld, gd = dev_in
-        rc = binding.attn_bwd_raw(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(),
-                                  gd.data_ptr(), ld.data_ptr(),
-                                  *(t.data_ptr() for t in dev_out), w.B, w.h, w.n_q, w.n_k,
-                                  w.d, w.scale, w.mask, None if dkl is None else dkl.data_ptr(),
-                                  ws.data_ptr(), ws_bytes, sptr)
+        if w.mask == inputs.MASK_BAND:
+            rc = binding.attn_bwd_window_raw(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(),
+                                             od.data_ptr(), gd.data_ptr(), ld.data_ptr(),
+                                             *(t.data_ptr() for t in dev_out), w.B, w.h, w.n_q,
+                                             w.n_k, w.d, w.scale, w.win_left, w.win_right,
+                                             ws.data_ptr(), ws_bytes, sptr)
+        else:
+            rc = binding.attn_bwd_raw(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(),
+                                      gd.data_ptr(), ld.data_ptr(),
+                                      *(t.data_ptr() for t in dev_out), w.B, w.h, w.n_q, w.n_k,
+                                      w.d, w.scale, w.mask,
+                                      None if dkl is None else dkl.data_ptr(), ws.data_ptr(),
+                                      ws_bytes, sptr)
         if rc != 0:
             raise binding.AttnError(rc, "attn_bwd")
         for h, d in zip(host_out, dev_out):

@@ -210,6 +210,19 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              int d_k, float scale, int mask_kind, const int* key_lens, void* workspace,
              size_t workspace_bytes, struct CUstream_st* stream);
 
+/*
+ * attn_bwd_window -- the gradients of attn_fwd_window (restricted
+ * self-attention: query i sees keys i - window_left .. i + window_right).
+ * Arguments as attn_bwd with mask_kind and key_lens replaced by the window
+ * sides (>= 0, else ATTN_ERR_INVALID_ARG); o and lse must come from
+ * attn_fwd_window with the same window.  Keys no query's window reaches get
+ * dk = dv = 0; queries whose window holds no key get dq = 0.
+ */
+int attn_bwd_window(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, int B, int h, int n_q,
+                    int n_k, int d_k, float scale, int window_left, int window_right,
+                    void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
 /* Scratch bytes attn_bwd needs for these sizes (0 for unsupported sizes). */
 size_t attn_bwd_workspace_bytes(int B, int h, int n_q, int d_k);
 

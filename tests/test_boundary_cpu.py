@@ -182,3 +182,17 @@ def test_strided_arguments_rejected_on_host(lib):
     assert call(mask=2, lens=None) == INV
     assert call(q=None) == INV
     assert call(d=48) == binding.ATTN_ERR_UNSUPPORTED
+
+
+def test_bwd_window_arguments_rejected_on_host(lib):
+    def call(left=4, right=4, d=64, q=A, ws_bytes=1 << 30):
+        return binding.attn_bwd_window_raw(q, A, A, A, A, A, A, A, A, 1, 1, 8, 8, d, 0.125, left,
+                                           right, A, ws_bytes, None)
+    INV = binding.ATTN_ERR_INVALID_ARG
+    assert call(left=-1) == INV and call(right=-1) == INV
+    assert call(q=None) == INV
+    assert call(ws_bytes=16) == INV
+    assert call(d=32) == binding.ATTN_ERR_UNSUPPORTED
+    # attn_bwd itself takes no window
+    assert binding.attn_bwd_raw(A, A, A, A, A, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 3, None, A,
+                                1 << 30, None) == INV

@@ -182,3 +182,54 @@ def test_bwd_full_size_sampled_heads(name):
     if w.mask == MASK_NONE:
         dks = dk.float().sum(dim=2)
         assert dks.abs().max().item() <= 0.05 * dk.float().abs().max().item() * math.sqrt(w.n_k)
+
+
+# ---------------------------------------------------------------- restricted window
+
+WINDOW_CASES = [
+    # B, h, n_q, n_k, left, right
+    (1, 2, 300, 300, 64, 64),
+    (1, 2, 512, 512, 128, 0),     # causal window
+    (2, 1, 200, 333, 0, 50),
+    (1, 1, 700, 100, 20, 20),     # queries past the last key: empty windows
+    (1, 2, 640, 640, 127, 129),   # window edges one off the tile size
+]
+
+
+@pytest.mark.parametrize("B,h,n_q,n_k,left,right", WINDOW_CASES)
+def test_bwd_window_matches_oracle(B, h, n_q, n_k, left, right):
+    q, k, v, g = _problem(B, h, n_q, n_k, seed=2)
+    qc, kc, vc, gc = (t.cuda() for t in (q, k, v, g))
+    o, lse = binding.attn_fwd_window(qc, kc, vc, left, right)
+    grads = binding.attn_bwd(qc, kc, vc, o, lse, gc, window=(left, right))
+    binding.check()
+    want = oracle.attn_bwd_band(q, k, v, g, 0.125, left, right)
+    _compare([t.float().cpu().numpy().astype(np.float64) for t in grads], want)
+
+
+def test_bwd_window_wide_equals_unmasked_bit_for_bit():
+    q, k, v, g = (t.cuda() for t in _problem(1, 2, 384, 384, seed=6))
+    o, lse = binding.attn_fwd(q, k, v)
+    a = binding.attn_bwd(q, k, v, o, lse, g, window=(10 ** 6, 10 ** 6))
+    b = binding.attn_bwd(q, k, v, o, lse, g)
+    binding.check()
+    # dK and dV accumulate inside one CTA each in the same order
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+def test_bwd_window_full_size_sampled_heads():
+    w = inputs.WORKLOADS["big_window"]
+    q, k, v, _ = inputs.make_inputs(w, device="cuda")
+    g = inputs.gaussian((w.B, w.h, w.n_q, w.d), 4).to(torch.bfloat16).cuda()
+    o, lse = binding.attn_fwd_window(q, k, v, w.win_left, w.win_right)
+    dq, dk, dv = binding.attn_bwd(q, k, v, o, lse, g, window=(w.win_left, w.win_right))
+    binding.check()
+    sel = [0, w.B * w.h - 1]
+    b_idx, h_idx = [s // w.h for s in sel], [s % w.h for s in sel]
+
+    def pick(t):
+        return t[b_idx, h_idx].unsqueeze(1).cpu()
+
+    want = oracle.attn_bwd_band(pick(q), pick(k), pick(v), pick(g), w.scale, w.win_left,
+                                w.win_right)
+    _compare([pick(t).float().numpy().astype(np.float64) for t in (dq, dk, dv)], want)

@@ -30,7 +30,7 @@ DECODE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 # Every entry point declared in include/attn.h.
 EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_fwd_window", "attn_fwd_strided", "attn_decode", "attn_decode_workspace_bytes",
-           "attn_decode_noalloc", "attn_bwd", "attn_bwd_workspace_bytes",
+           "attn_decode_noalloc", "attn_bwd", "attn_bwd_window", "attn_bwd_workspace_bytes",
            "attn_check", "attn_status_string",
            "attn_last_cuda_error", "attn_set_wait_limit_ns", "attn_launch_count",
            "attn_diag_tile", "attn_diag_wait_timeout")
@@ -80,6 +80,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         lib.attn_bwd.restype = i32
         lib.attn_bwd.argtypes = [vp] * 9 + [i32] * 5 + [f32, i32, vp, vp, ctypes.c_size_t, vp]
+        lib.attn_bwd_window.restype = i32
+        lib.attn_bwd_window.argtypes = [vp] * 9 + [i32] * 5 + [f32, i32, i32, vp, ctypes.c_size_t,
+                                                                vp]
         lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32]
         lib.attn_check.restype = i32
@@ -319,16 +322,27 @@ def attn_bwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, dout_ptr, lse_ptr, dq_ptr, dk_ptr, 
                            int(ws_bytes), stream_ptr)
 
 
+def attn_bwd_window_raw(q_ptr, k_ptr, v_ptr, o_ptr, dout_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr, B,
+                        h, n_q, n_k, d, scale, left, right, ws_ptr, ws_bytes, stream_ptr) -> int:
+    """The C call itself, on raw device pointers; returns the status code."""
+    return load().attn_bwd_window(q_ptr, k_ptr, v_ptr, o_ptr, dout_ptr, lse_ptr, dq_ptr, dk_ptr,
+                                  dv_ptr, B, h, n_q, n_k, d, float(scale), int(left), int(right),
+                                  ws_ptr, int(ws_bytes), stream_ptr)
+
+
 def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              lse: torch.Tensor, dout: torch.Tensor, scale: float | None = None,
              mask: int = MASK_NONE, key_lens: torch.Tensor | None = None,
              dq: torch.Tensor | None = None, dk: torch.Tensor | None = None,
-             dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+             dv: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+             window: tuple[int, int] | None = None, stream=None):
     """Gradients (dq, dk, dv) of attn_fwd for dout = dLoss/dO.
 
     q, k, v, o, dout: contiguous bf16 CUDA [B, h, n, 64] tensors; o and lse
     are what attn_fwd returned for q, k, v with the same scale and mask.
     A workspace of bwd_workspace_bytes(...) is allocated when none is given.
+    ``window=(left, right)`` differentiates attn_fwd_window instead (mask and
+    key_lens ignored).
     """
     for t in (q, k, v, o, dout):
         if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
@@ -358,11 +372,17 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    rc = attn_bwd_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
-                      _ptr(dk), _ptr(dv), B, h, n_q, n_k, d, scale, int(mask), _ptr(kl),
-                      _ptr(workspace), ws_bytes, _stream_ptr(stream))
+    if window is not None:
+        rc = attn_bwd_window_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), B, h, n_q, n_k, d, scale,
+                                 window[0], window[1], _ptr(workspace), ws_bytes,
+                                 _stream_ptr(stream))
+    else:
+        rc = attn_bwd_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                          _ptr(dk), _ptr(dv), B, h, n_q, n_k, d, scale, int(mask), _ptr(kl),
+                          _ptr(workspace), ws_bytes, _stream_ptr(stream))
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_bwd")
+        raise AttnError(rc, "attn_bwd_window" if window is not None else "attn_bwd")
     return dq, dk, dv
 
 

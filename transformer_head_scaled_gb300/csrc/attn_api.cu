@@ -426,11 +426,18 @@ size_t attn_bwd_workspace_bytes(int B, int h, int n_q, int d_k) {
   return bwd_layout(B, h, n_q).bytes;
 }
 
-int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-             const float* lse, void* dq, void* dk, void* dv, int B, int h, int n_q, int n_k,
-             int d_k, float scale, int mask_kind, const int* key_lens, void* workspace,
-             size_t workspace_bytes, struct CUstream_st* stream) {
-  int rc = check_common(q, k, v, o, lse, B, h, n_q, n_k, d_k, scale, mask_kind, key_lens, 2);
+}  // extern "C"
+
+namespace attn {
+namespace {
+static int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, int B, int h, int n_q,
+                    int n_k, int d_k, float scale, int mask_kind, const int* key_lens,
+                    int window_left, int window_right, void* workspace, size_t workspace_bytes,
+                    struct CUstream_st* stream) {
+  const bool window = mask_kind == kMaskBand;
+  int rc = check_common(q, k, v, o, lse, B, h, n_q, n_k, d_k, scale,
+                        window ? ATTN_MASK_NONE : mask_kind, key_lens, 2);
   if (rc != ATTN_OK) return rc;
   if (!dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
@@ -452,12 +459,37 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if ((rc = encode_3d_f32(&maps[6], static_cast<uint8_t*>(workspace) + lay.dq_acc_off, n_q, bh)) !=
       ATTN_OK)
     return rc;
+  const int reach = n_q + n_k;
   BwdProblem pb{q, k, v, o, dout, lse, dq, dk, dv, B, h, n_q, n_k, scale, mask_kind,
-                mask_kind == ATTN_MASK_KEY_PADDING ? key_lens : nullptr};
+                mask_kind == ATTN_MASK_KEY_PADDING ? key_lens : nullptr,
+                window_left < reach ? window_left : reach,
+                window_right < reach ? window_right : reach};
   cudaError_t e = launch_bwd(pb, maps, workspace, make_ctx(*di, stream));
   if (e != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(3);
   return ATTN_OK;
+}
+}  // namespace
+}  // namespace attn
+
+extern "C" {
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int B, int h, int n_q, int n_k,
+             int d_k, float scale, int mask_kind, const int* key_lens, void* workspace,
+             size_t workspace_bytes, struct CUstream_st* stream) {
+  if (mask_kind == ATTN_MASK_WINDOW) return ATTN_ERR_INVALID_ARG;  // attn_bwd_window
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, h, n_q, n_k, d_k, scale, mask_kind,
+                  key_lens, 0, 0, workspace, workspace_bytes, stream);
+}
+
+int attn_bwd_window(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, int B, int h, int n_q,
+                    int n_k, int d_k, float scale, int window_left, int window_right,
+                    void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
+  if (window_left < 0 || window_right < 0) return ATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, h, n_q, n_k, d_k, scale, kMaskBand,
+                  nullptr, window_left, window_right, workspace, workspace_bytes, stream);
 }
 
 int attn_check(struct CUstream_st* stream) {

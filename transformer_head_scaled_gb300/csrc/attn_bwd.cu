@@ -126,6 +126,7 @@ struct Params {
   const int* key_lens;
   int H, n_q, n_k, BH;
   int mask;
+  int win_left, win_right;  // restricted attention: query i sees keys i - left .. i + right
   int num_qt, num_kt, num_items;
   float scale_log2;  // scale * log2(e)
   float scale;
@@ -163,6 +164,14 @@ __device__ __forceinline__ Item bwd_item(const Params& p, int t) {
       // query i sees key j iff j <= i: tiles before kt see none of these keys
       it.qt0 = it.kt;
       it.n = max(p.num_qt - it.kt, 0);
+    } else if (p.mask == kMaskBand) {
+      // key j is seen by the queries j - right .. j + left
+      const int j_lo = it.kt * BN, j_hi = min(j_lo + BN - 1, limit - 1);
+      const int q_lo = max(j_lo - p.win_right, 0), q_hi = min(j_hi + p.win_left, p.n_q - 1);
+      if (q_lo <= q_hi) {
+        it.qt0 = q_lo / BM;
+        it.n = q_hi / BM - it.qt0 + 1;
+      }
     } else {
       it.n = p.num_qt;
     }
@@ -232,6 +241,9 @@ __device__ __forceinline__ void st_row_sw128(uint32_t tile, int r, const uint32_
                  w[first_word + 4 * g + 2], w[first_word + 4 * g + 3]);
 }
 
+// BAND = restricted self-attention (its own instantiation, so that the
+// window's two extra compares per score stay out of the other masks' code).
+template <bool BAND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk,
@@ -656,12 +668,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int i = 0; i < item.n; ++i, ++t) {
         const int qt = item.qt0 + i;
         // leading columns whose query precedes this key (causal diagonal
-        // tile), or all of them for a key past the sequence
-        int lim = 0;
+        // tile), or all of them for a key past the sequence; with the window,
+        // the columns outside [lim, hi) (queries i with j < i - left or
+        // j > i + right)
+        int lim = 0, hi = 64;
         if (!row_valid) {
           lim = 64;
         } else if (p.mask == kMaskCausal && qt == item.kt) {
           lim = min(max(r - 64 * half, 0), 64);
+        } else if (BAND) {
+          const int qbase = qt * BM + 64 * half;
+          lim = min(max(j - p.win_right - qbase, 0), 64);
+          hi = min(max(j + p.win_left - qbase + 1, 0), 64);
         }
         if (!wait(&sm.s_full, t & 1)) break;
         tc_fence_after();
@@ -683,10 +701,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           fma2(x0, x1, __uint_as_float(src[0]), __uint_as_float(src[1]), c, c, 0.f, 0.f);
           fma2(x2, x3, __uint_as_float(src[2]), __uint_as_float(src[3]), c, c, 0.f, 0.f);
           const int c0 = 2 * i2;
-          pf[c0 + 0] = c0 + 0 < lim ? 0.f : ex2(x0);
-          pf[c0 + 1] = c0 + 1 < lim ? 0.f : ex2(x1);
-          pf[c0 + 2] = c0 + 2 < lim ? 0.f : ex2(x2);
-          pf[c0 + 3] = c0 + 3 < lim ? 0.f : ex2(x3);
+          pf[c0 + 0] = (c0 + 0 < lim || (BAND && c0 + 0 >= hi)) ? 0.f : ex2(x0);
+          pf[c0 + 1] = (c0 + 1 < lim || (BAND && c0 + 1 >= hi)) ? 0.f : ex2(x1);
+          pf[c0 + 2] = (c0 + 2 < lim || (BAND && c0 + 2 >= hi)) ? 0.f : ex2(x2);
+          pf[c0 + 3] = (c0 + 3 < lim || (BAND && c0 + 3 >= hi)) ? 0.f : ex2(x3);
         }
         uint32_t w[32];
 #pragma unroll
@@ -871,6 +889,8 @@ cudaError_t launch_bwd(const BwdProblem& pb, const CUtensorMap* maps, void* work
   p.n_k = pb.n_k;
   p.BH = static_cast<int>(bh);
   p.mask = pb.mask;
+  p.win_left = pb.win_left;
+  p.win_right = pb.win_right;
   p.num_qt = (pb.n_q + BM - 1) / BM;
   p.num_kt = (pb.n_k + BN - 1) / BN;
   p.num_items = p.BH * p.num_kt;
@@ -879,12 +899,18 @@ cudaError_t launch_bwd(const BwdProblem& pb, const CUtensorMap* maps, void* work
   p.limit_ns = ctx.limit_ns;
   p.status = ctx.status;
   const size_t smem = bwd_tc_smem_bytes();
-  err = cudaFuncSetAttribute(attn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+  const bool band = pb.mask == kMaskBand;
+  err = cudaFuncSetAttribute(band ? reinterpret_cast<const void*>(attn_bwd_tc_kernel<true>)
+                                  : reinterpret_cast<const void*>(attn_bwd_tc_kernel<false>),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int grid = p.num_items < ctx.num_sms ? p.num_items : ctx.num_sms;
-  attn_bwd_tc_kernel<<<grid, NUM_THREADS, smem, ctx.stream>>>(maps[0], maps[1], maps[2], maps[3],
-                                                              maps[4], maps[5], maps[6], p);
+  if (band)
+    attn_bwd_tc_kernel<true><<<grid, NUM_THREADS, smem, ctx.stream>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], p);
+  else
+    attn_bwd_tc_kernel<false><<<grid, NUM_THREADS, smem, ctx.stream>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 

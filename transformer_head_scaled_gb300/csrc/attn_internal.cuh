@@ -89,6 +89,7 @@ struct BwdProblem {
   float scale;
   int mask;
   const int* key_lens;
+  int win_left, win_right;  // kMaskBand: query i sees keys i - win_left .. i + win_right
 };
 
 // Workspace of the backward: the per-query constant tiles (one [128 x 16]

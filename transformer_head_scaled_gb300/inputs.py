@@ -114,6 +114,9 @@ WORKLOADS = {
                         note="backward, big model, long sequence"),
     "big_causal_bwd": Workload("big_causal_bwd", 8, 16, 4096, 4096, 64, MASK_CAUSAL, "bf16",
                                kind="bwd", note="backward, big model, long sequence, causal"),
+    "big_window_bwd": Workload("big_window_bwd", 8, 16, 4096, 4096, 64, MASK_BAND, "bf16",
+                               win_left=256, win_right=256, kind="bwd",
+                               note="backward of restricted self-attention, window of 513"),
 }
 
 
