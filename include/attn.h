@@ -191,7 +191,8 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
  * This is the back-propagation through eq. (1) of "Attention Is All You
  * Need" (section 3.2.1) that training the model (section 5) needs; the
  * paper does not write it out.
- *   q, k, v  : bf16, as for attn_fwd (d_k must be 64, else ATTN_ERR_UNSUPPORTED).
+ *   q, k, v  : bf16, as for attn_fwd; d_k = d_v in {16, 32, 64}, else
+ *              ATTN_ERR_UNSUPPORTED (d_k = 128 is forward-only).
  *   o, lse   : the output and log-sum-exp attn_fwd returned for these inputs
  *              (lse is required here).
  *   dout     : bf16 [B, h, n_q, d_k].

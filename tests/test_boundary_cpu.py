@@ -142,7 +142,7 @@ def test_bwd_arguments_rejected_on_host(lib):
     assert call(n_q=0) == INV and call(n_k=0) == INV and call(B=0) == INV and call(h=-1) == INV
     assert call(scale=0.0) == INV and call(scale=float("nan")) == INV
     assert call(mask=2) == INV and call(mask=5) == INV
-    assert call(d=32) == UNS
+    assert call(d=48) == UNS and call(d=128) == UNS and call(d=8) == UNS
     need = lib.attn_bwd_workspace_bytes(2, 3, 200, 64)
     assert call(B=2, h=3, n_q=200, ws_bytes=need - 1) == INV
 
@@ -152,7 +152,11 @@ def test_bwd_workspace_size():
     # per head and 128-query tile a 4 KB constant tile, then n_q x 64 float32
     assert binding.bwd_workspace_bytes(2, 3, 200) == 6 * (2 * 4096 + 200 * 64 * 4)
     assert binding.bwd_workspace_bytes(1, 1, 128) == 4096 + 128 * 64 * 4
-    assert binding.bwd_workspace_bytes(1, 1, 8, 32) == 0
+    # d = 16, 32: the same constant tiles, n_q x d float32
+    assert binding.bwd_workspace_bytes(1, 1, 8, 32) == 4096 + 8 * 32 * 4
+    assert binding.bwd_workspace_bytes(2, 1, 300, 16) == 2 * (3 * 4096 + 300 * 16 * 4)
+    assert binding.bwd_workspace_bytes(1, 1, 8, 128) == 0
+    assert binding.bwd_workspace_bytes(1, 1, 8, 48) == 0
     assert binding.bwd_workspace_bytes(0, 1, 8) == 0
 
 
@@ -192,7 +196,7 @@ def test_bwd_window_arguments_rejected_on_host(lib):
     assert call(left=-1) == INV and call(right=-1) == INV
     assert call(q=None) == INV
     assert call(ws_bytes=16) == INV
-    assert call(d=32) == binding.ATTN_ERR_UNSUPPORTED
+    assert call(d=128) == binding.ATTN_ERR_UNSUPPORTED
     # attn_bwd itself takes no window
     assert binding.attn_bwd_raw(A, A, A, A, A, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 3, None, A,
                                 1 << 30, None) == INV

@@ -45,11 +45,11 @@ def _bf16(shape, seed):
     return inputs.gaussian(shape, seed).to(torch.bfloat16)
 
 
-def _problem(B, h, n_q, n_k, seed=0):
-    q = _bf16((B, h, n_q, 64), seed)
-    k = _bf16((B, h, n_k, 64), seed + 1)
-    v = _bf16((B, h, n_k, 64), seed + 2)
-    g = _bf16((B, h, n_q, 64), seed + 3)
+def _problem(B, h, n_q, n_k, seed=0, d=64):
+    q = _bf16((B, h, n_q, d), seed)
+    k = _bf16((B, h, n_k, d), seed + 1)
+    v = _bf16((B, h, n_k, d), seed + 2)
+    g = _bf16((B, h, n_q, d), seed + 3)
     return q, k, v, g
 
 
@@ -152,7 +152,8 @@ def test_bwd_launch_count():
     assert binding.launch_count() - before == 3
 
 
-@pytest.mark.parametrize("name", ["base_enc", "base_dec", "encdec", "big"])
+@pytest.mark.parametrize("name", ["base_enc", "base_dec", "encdec", "big", "base_h16_d32",
+                                  "base_h32_d16"])
 def test_bwd_full_size_sampled_heads(name):
     """Full-size workloads in the launch configuration the benchmark times;
     the oracle recomputes a few whole heads (first, last and random ones)."""
@@ -233,3 +234,37 @@ def test_bwd_window_full_size_sampled_heads():
     want = oracle.attn_bwd_band(pick(q), pick(k), pick(v), pick(g), w.scale, w.win_left,
                                 w.win_right)
     _compare([pick(t).float().numpy().astype(np.float64) for t in (dq, dk, dv)], want)
+
+
+# ---------------------------------------------------------------- other head sizes
+
+HEAD_SIZE_CASES = [
+    # B, h, n_q, n_k, mask, lens
+    (1, 2, 128, 128, MASK_NONE, None),
+    (2, 3, 200, 328, MASK_NONE, None),
+    (2, 2, 300, 300, MASK_CAUSAL, None),
+    (1, 1, 384, 200, MASK_CAUSAL, None),
+    (3, 2, 100, 330, MASK_KEY_PADDING, [128, 0, 301]),
+]
+
+
+@pytest.mark.parametrize("d", [16, 32])
+@pytest.mark.parametrize("B,h,n_q,n_k,mask,lens", HEAD_SIZE_CASES)
+def test_bwd_head_sizes_match_oracle(d, B, h, n_q, n_k, mask, lens):
+    q, k, v, g = _problem(B, h, n_q, n_k, seed=11, d=d)
+    scale = 1 / math.sqrt(d)
+    got = _gpu_grads(q, k, v, g, mask, lens, scale)
+    want = oracle.attn_bwd(q, k, v, g, scale, mask, None if lens is None else np.array(lens))
+    _compare(got, want)
+
+
+@pytest.mark.parametrize("d", [16, 32])
+def test_bwd_head_sizes_window_matches_oracle(d):
+    q, k, v, g = _problem(1, 2, 640, 640, seed=12, d=d)
+    scale = 1 / math.sqrt(d)
+    qc, kc, vc, gc = (t.cuda() for t in (q, k, v, g))
+    o, lse = binding.attn_fwd_window(qc, kc, vc, 127, 129, scale=scale)
+    grads = binding.attn_bwd(qc, kc, vc, o, lse, gc, scale=scale, window=(127, 129))
+    binding.check()
+    want = oracle.attn_bwd_band(q, k, v, g, scale, 127, 129)
+    _compare([t.float().cpu().numpy().astype(np.float64) for t in grads], want)

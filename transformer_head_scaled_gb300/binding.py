@@ -182,7 +182,8 @@ def attn_fwd_window(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, left: int
                     lse: torch.Tensor | None = None, with_lse: bool = True, stream=None):
     """Restricted self-attention on the GPU: query i sees keys i-left .. i+right.
 
-    q, k, v: contiguous bf16 CUDA [B, h, n, 64] tensors.  Returns (o, lse).
+    q, k, v: contiguous bf16 CUDA [B, h, n, d] tensors, d in {16, 32, 64, 128}.
+    Returns (o, lse).
     """
     for t in (q, k, v):
         if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
@@ -338,8 +339,9 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              window: tuple[int, int] | None = None, stream=None):
     """Gradients (dq, dk, dv) of attn_fwd for dout = dLoss/dO.
 
-    q, k, v, o, dout: contiguous bf16 CUDA [B, h, n, 64] tensors; o and lse
-    are what attn_fwd returned for q, k, v with the same scale and mask.
+    q, k, v, o, dout: contiguous bf16 CUDA [B, h, n, d] tensors, d in {16, 32,
+    64}; o and lse are what attn_fwd returned for q, k, v with the same scale
+    and mask.
     A workspace of bwd_workspace_bytes(...) is allocated when none is given.
     ``window=(left, right)`` differentiates attn_fwd_window instead (mask and
     key_lens ignored).

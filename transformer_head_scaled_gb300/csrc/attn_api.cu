@@ -126,17 +126,23 @@ int encode_3d(CUtensorMap* map, const void* base, int d, int n, long long bh, in
   return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
 }
 
-// (64, n, B*H) fp32 view with a (32, 64, 1) box and 128-byte swizzle (the
-// backward's dQ accumulator, added into by TMA reduce).
-int encode_3d_f32(CUtensorMap* map, const void* base, int n, long long bh) {
-  cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(bh)};
-  cuuint64_t strides[2] = {256u, 256u * static_cast<cuuint64_t>(n)};
-  cuuint32_t box[3] = {32u, 64u, 1u};
+// (d, n, B*H) fp32 view with a (min(d, 32), 64, 1) box in the swizzle of its
+// 4*min(d, 32)-byte rows (the backward's dQ accumulator, added into by TMA
+// reduce).
+int encode_3d_f32(CUtensorMap* map, const void* base, int d, int n, long long bh) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
+                        static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                           static_cast<cuuint64_t>(d) * 4 * static_cast<cuuint64_t>(n)};
+  const int inner = d < 32 ? d : 32;
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(inner), 64u, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUtensorMapSwizzle swz = inner == 32   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : inner == 16 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_32B;
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
 }
 
@@ -421,9 +427,9 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
 }
 
 size_t attn_bwd_workspace_bytes(int B, int h, int n_q, int d_k) {
-  if (B < 1 || h < 1 || n_q < 1 || d_k != 64) return 0;
+  if (B < 1 || h < 1 || n_q < 1 || !bwd_head_size_ok(d_k)) return 0;
   if (static_cast<long long>(B) * h > 0x7fffffffLL) return 0;
-  return bwd_layout(B, h, n_q).bytes;
+  return bwd_layout(B, h, n_q, d_k).bytes;
 }
 
 }  // extern "C"
@@ -443,8 +449,8 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
   if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       !aligned16(workspace))
     return ATTN_ERR_INVALID_ARG;
-  if (d_k != 64) return ATTN_ERR_UNSUPPORTED;
-  const BwdLayout lay = bwd_layout(B, h, n_q);
+  if (!bwd_head_size_ok(d_k)) return ATTN_ERR_UNSUPPORTED;
+  const BwdLayout lay = bwd_layout(B, h, n_q, d_k);
   if (workspace_bytes < lay.bytes) return ATTN_ERR_INVALID_ARG;
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di)) != ATTN_OK) return rc;
@@ -456,11 +462,11 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
   if ((rc = encode_3d(&maps[3], dout, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
   if ((rc = encode_3d(&maps[4], dk, d_k, n_k, bh, 64)) != ATTN_OK) return rc;
   if ((rc = encode_3d(&maps[5], dv, d_k, n_k, bh, 64)) != ATTN_OK) return rc;
-  if ((rc = encode_3d_f32(&maps[6], static_cast<uint8_t*>(workspace) + lay.dq_acc_off, n_q, bh)) !=
-      ATTN_OK)
+  if ((rc = encode_3d_f32(&maps[6], static_cast<uint8_t*>(workspace) + lay.dq_acc_off, d_k, n_q,
+                          bh)) != ATTN_OK)
     return rc;
   const int reach = n_q + n_k;
-  BwdProblem pb{q, k, v, o, dout, lse, dq, dk, dv, B, h, n_q, n_k, scale, mask_kind,
+  BwdProblem pb{q, k, v, o, dout, lse, dq, dk, dv, B, h, n_q, n_k, d_k, scale, mask_kind,
                 mask_kind == ATTN_MASK_KEY_PADDING ? key_lens : nullptr,
                 window_left < reach ? window_left : reach,
                 window_right < reach ? window_right : reach};

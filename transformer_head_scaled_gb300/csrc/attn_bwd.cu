@@ -68,8 +68,7 @@ using namespace ptx;
 
 constexpr int BM = 128;  // queries per query tile
 constexpr int BN = 128;  // keys per key tile (= tensor-memory lanes)
-constexpr int D = 64;    // head size
-constexpr uint32_t TILE_BYTES = 128 * D * 2;  // a [128 x 64] bf16 tile: 16 KB
+constexpr uint32_t DS_BLOCK = 128 * 64 * 2;  // a [128 x 64] bf16 block of dS^T: 16 KB
 // Q (and its constant tile) ring: Q is last read by dK, late in a tile pair,
 // so three stages let the next tile's loads start two tile pairs ahead.  dO
 // is last read by dV, early in a tile pair: two stages suffice.
@@ -80,8 +79,7 @@ constexpr int EPI_WARP0 = 8;
 constexpr int LOAD_WARP = 12;
 constexpr int MMA_WARP = 13;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 320, COL_DQ = 384,
-                   COL_PT = 448;
+constexpr uint32_t COL_S = 0, COL_DP = 128;
 // The [128 x 16] bf16 constant tile of a query tile (K-major, no swizzle:
 // 8-row x 16-byte core matrices, the second 8 columns 128 B after the first,
 // 8-row groups 256 B apart).  Row i holds b_i in columns 0-2 (hi, mid, lo)
@@ -91,21 +89,40 @@ constexpr float LOG2E = 1.4426950408889634f;
 
 static_assert(BM == BN, "the causal tile range assumes square tiles");
 
-constexpr uint32_t HALF_TILE_BYTES = TILE_BYTES / 2;  // 64 rows x 128 bytes
+constexpr uint32_t STAGE_BYTES = 64 * 128;  // an epilogue staging buffer: 64 rows x 128 bytes
 constexpr int EPI_BAR0 = 1;  // named barriers 1, 2: the two epilogue groups
 
+// Shapes per head size d (16, 32, 64; d_k = d_v): Q, K, V and dO tiles of
+// [128 x d] bf16 with rows of 2d bytes in the widest swizzle they fit; dV,
+// dK and dQ accumulators of max(d, 32) tensor-memory columns (32-column
+// loads never touch a neighbour); dQ added into the fp32 accumulator in boxes
+// of min(d, 32) columns.  (d = 128 would need 704 tensor-memory columns.)
+template <int D_>
+struct BCfg {
+  static constexpr uint32_t RB = D_ * 2;
+  static constexpr uint32_t SWZ = RB == 128 ? 2u : (RB == 64 ? 4u : 6u);
+  static constexpr uint32_t TILE = 128 * D_ * 2;
+  static constexpr uint32_t OW = D_ < 32 ? 32 : D_;
+  static constexpr uint32_t COL_DV = 256, COL_DK = 256 + OW, COL_DQ = 256 + 2 * OW,
+                            COL_PT = 256 + 3 * OW;
+  static constexpr uint32_t QRB = (D_ < 32 ? D_ : 32) * 4;  // row bytes of a dQ box
+  static_assert(COL_PT + 64 <= 512, "tensor memory");
+};
+
+template <int D_>
 struct __align__(1024) Smem {
-  uint8_t k[2][TILE_BYTES];
-  uint8_t v[TILE_BYTES];
-  uint8_t q[QSTAGES][TILE_BYTES];
-  uint8_t dout[OSTAGES][TILE_BYTES];
+  using C = BCfg<D_>;
+  uint8_t k[2][C::TILE];
+  uint8_t v[C::TILE];
+  uint8_t q[QSTAGES][C::TILE];
+  uint8_t dout[OSTAGES][C::TILE];
   // dS^T as [128 keys x 128 queries] bf16, two buffers (tile pairs t even /
   // odd), each two 64-query column blocks of [128 x 64] in the 128-byte
   // swizzled layout.
-  uint8_t dst[2][2][TILE_BYTES];
-  // epilogue staging, one 64-row buffer per epilogue group: a 32-column fp32
-  // half of dQ, or dV / dK in bf16, 128-byte swizzled
-  uint8_t stage[2][HALF_TILE_BYTES];
+  uint8_t dst[2][2][DS_BLOCK];
+  // epilogue staging, one 64-row buffer per epilogue group: a fp32 box of
+  // dQ, or dV / dK in bf16, swizzled as the tensor map it is copied with
+  uint8_t stage[2][STAGE_BYTES];
   uint8_t cst[QSTAGES][CONST_TILE_BYTES];  // the constant tile of each Q stage
   // Two 8 x 8 bf16 core matrices that select columns of the constant tile:
   // [0] rows (1,1,1,0,0,0,0,0) picks b, [1] rows (0,0,0,1,1,1,0,0) picks -D.
@@ -188,7 +205,8 @@ __device__ __forceinline__ int next_item(const Params& p, int from, Item& out) {
   return -1;
 }
 
-__device__ __forceinline__ void record_timeout(const Params& p, Smem& sm) {
+template <class SmemT>
+__device__ __forceinline__ void record_timeout(const Params& p, SmemT& sm) {
   atomicCAS(p.status, kDevOk, kDevTimeout);
   *reinterpret_cast<volatile int*>(&sm.abort) = 1;
 }
@@ -230,20 +248,34 @@ __device__ __forceinline__ uint64_t sdesc_plain(uint32_t smem_addr, uint32_t lbo
   return d;
 }
 
-// One row (128 bytes = eight 16-byte chunks) into a 128-byte swizzled tile:
-// chunk g of row r lands at chunk position g ^ (r % 8).
-__device__ __forceinline__ void st_row_sw128(uint32_t tile, int r, const uint32_t (&w)[32],
-                                             int first_word) {
-  const uint32_t base = tile + r * 128;
+// One row of RBYTES (128, 64 or 32) into a tile swizzled at that width:
+// 16-byte chunk g of row r lands at chunk position g ^ ((r * RBYTES / 128) %
+// (RBYTES / 16)), the layout a TMA copy with that swizzle reads and writes.
+template <uint32_t RBYTES>
+__device__ __forceinline__ void st_row_swz(uint32_t tile, int r, const uint32_t (&w)[32]) {
+  const uint32_t base = tile + r * RBYTES;
+  const uint32_t x = ((static_cast<uint32_t>(r) * RBYTES) >> 7) & (RBYTES / 16 - 1);
 #pragma unroll
-  for (int g = 0; g < 8; ++g)
-    st_shared_v4(base + ((g ^ (r & 7)) << 4), w[first_word + 4 * g], w[first_word + 4 * g + 1],
-                 w[first_word + 4 * g + 2], w[first_word + 4 * g + 3]);
+  for (uint32_t g = 0; g < RBYTES / 16; ++g)
+    st_shared_v4(base + ((g ^ x) << 4), w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+}
+
+// Shared-memory matrix descriptor (same fields as sdesc_sw128) with the
+// layout code `swz` at bits 61-63.
+__device__ __forceinline__ uint64_t sdesc_swz(uint32_t smem_addr, uint32_t lbo_bytes,
+                                              uint32_t sbo_bytes, uint32_t swz) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= static_cast<uint64_t>(swz) << 61;
+  return d;
 }
 
 // BAND = restricted self-attention (its own instantiation, so that the
 // window's two extra compares per score stay out of the other masks' code).
-template <bool BAND>
+template <bool BAND, int D_>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk,
@@ -252,9 +284,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        const __grid_constant__ CUtensorMap tmdk,
                        const __grid_constant__ CUtensorMap tmdv,
                        const __grid_constant__ CUtensorMap tmdq, const Params p) {
+  using C = BCfg<D_>;
+  constexpr int D = D_;
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~static_cast<uintptr_t>(1023));
+  Smem<D_>& sm = *reinterpret_cast<Smem<D_>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const volatile int* abort = &sm.abort;
@@ -330,7 +364,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t slot = it & 1;
         ok = mbar_wait(smem_u32(&sm.k_empty[slot]), ((it >> 1) & 1) ^ 1, p.limit_ns, abort);
         if (!ok) break;
-        mbar_arrive_expect_tx(smem_u32(&sm.k_full[slot]), TILE_BYTES);
+        mbar_arrive_expect_tx(smem_u32(&sm.k_full[slot]), C::TILE);
         tma_load_3d(smem_u32(sm.k[slot]), &tmk, smem_u32(&sm.k_full[slot]), 0, item.kt * BN,
                     item.bh);
         ++it;
@@ -340,7 +374,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = mbar_wait(smem_u32(&sm.q_empty[st]), ((nq / QSTAGES) & 1) ^ 1, p.limit_ns, abort);
           if (!ok) break;
           const uint32_t qb = smem_u32(&sm.q_full[st]);
-          mbar_arrive_expect_tx(qb, TILE_BYTES + CONST_TILE_BYTES);
+          mbar_arrive_expect_tx(qb, C::TILE + CONST_TILE_BYTES);
           tma_load_3d(smem_u32(sm.q[st]), &tmq, qb, 0, qt * BM, item.bh);
           const size_t tile = static_cast<size_t>(item.bh) * p.num_qt + qt;
           bulk_load(smem_u32(sm.cst[st]), p.cst + tile * CONST_TILE_BYTES, CONST_TILE_BYTES, qb);
@@ -349,7 +383,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // V of this item, once the previous item's last dP has read the slot
             ok = mbar_wait(smem_u32(&sm.v_empty), (nv & 1) ^ 1, p.limit_ns, abort);
             if (!ok) break;
-            mbar_arrive_expect_tx(smem_u32(&sm.v_full), TILE_BYTES);
+            mbar_arrive_expect_tx(smem_u32(&sm.v_full), C::TILE);
             tma_load_3d(smem_u32(sm.v), &tmv, smem_u32(&sm.v_full), 0, item.kt * BN, item.bh);
             ++nv;
           }
@@ -357,7 +391,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = mbar_wait(smem_u32(&sm.o_empty[os]), ((no / OSTAGES) & 1) ^ 1, p.limit_ns, abort);
           if (!ok) break;
           const uint32_t ob = smem_u32(&sm.o_full[os]);
-          mbar_arrive_expect_tx(ob, TILE_BYTES);
+          mbar_arrive_expect_tx(ob, C::TILE);
           tma_load_3d(smem_u32(sm.dout[os]), &tmdo, ob, 0, qt * BM, item.bh);
           ++no;
         }
@@ -386,25 +420,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr uint32_t IDESC_SQ = idesc_bf16_f32(BN, BM, false, false);  // S^T, dP^T
     constexpr uint32_t IDESC_KV = idesc_bf16_f32(BN, D, false, true);    // dV (A in tensor memory), dK
     constexpr uint32_t IDESC_DQ = idesc_bf16_f32(BM, D, true, true);     // dQ
-    constexpr uint32_t T16 = TILE_BYTES >> 4;                            // a tile in desc units
-    // K-major operands (rows x 64 bf16, 8-row groups 1024 B apart; a K step
-    // of 16 elements is +32 B = +2 inside the swizzle row).
-    const uint64_t kK = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);
-    const uint64_t kV = sdesc_sw128(smem_u32(sm.v), 16, 1024);
-    const uint64_t kQ = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
-    const uint64_t kDO = sdesc_sw128(smem_u32(sm.dout[0]), 16, 1024);
+    constexpr uint32_t T16 = C::TILE >> 4;     // a [128 x d] tile in desc units
+    constexpr uint32_t DS16 = DS_BLOCK >> 4;   // a dS^T column block in desc units
+    constexpr uint32_t RB16 = C::RB;           // 16 rows of RB bytes in desc units
+    // K-major operands (rows x d bf16, 8-row groups 8*RB bytes apart; a K
+    // step of 16 elements is +32 B = +2 inside the swizzle row).
+    const uint64_t kK = sdesc_swz(smem_u32(sm.k[0]), 16, 8 * C::RB, C::SWZ);
+    const uint64_t kV = sdesc_swz(smem_u32(sm.v), 16, 8 * C::RB, C::SWZ);
+    const uint64_t kQ = sdesc_swz(smem_u32(sm.q[0]), 16, 8 * C::RB, C::SWZ);
+    const uint64_t kDO = sdesc_swz(smem_u32(sm.dout[0]), 16, 8 * C::RB, C::SWZ);
     // dS^T as the K-major A operand of dK (M = keys, K = queries): a K step
     // inside a 64-query column block is +2, the second block is +16 KB.
     const uint64_t kDST = sdesc_sw128(smem_u32(sm.dst[0][0]), 16, 1024);
-    // MN-major B operands (K = the rows of the tile, N = the 64 columns): a K
-    // step of 16 rows is +2048 B = +128; 8-row groups 1024 B apart (SBO); N
-    // is one swizzle atom, LBO unused (set to 1024).
-    const uint64_t nQ = sdesc_sw128(smem_u32(sm.q[0]), 1024, 1024);
-    const uint64_t nDO = sdesc_sw128(smem_u32(sm.dout[0]), 1024, 1024);
-    const uint64_t nK = sdesc_sw128(smem_u32(sm.k[0]), 1024, 1024);
+    // MN-major B operands (K = the rows of the tile, N = the d columns): a K
+    // step of 16 rows is 16*RB bytes (+RB16); 8-row groups 8*RB bytes apart
+    // (SBO); N is one swizzle atom, LBO unused (set to 1024).
+    const uint64_t nQ = sdesc_swz(smem_u32(sm.q[0]), 1024, 8 * C::RB, C::SWZ);
+    const uint64_t nDO = sdesc_swz(smem_u32(sm.dout[0]), 1024, 8 * C::RB, C::SWZ);
+    const uint64_t nK = sdesc_swz(smem_u32(sm.k[0]), 1024, 8 * C::RB, C::SWZ);
     // dS as the MN-major A operand of dQ (M = queries across the two column
     // blocks, 16 KB apart = LBO; K = keys, 16 rows per step = +128).
-    const uint64_t nDS = sdesc_sw128(smem_u32(sm.dst[0][0]), TILE_BYTES, 1024);
+    const uint64_t nDS = sdesc_sw128(smem_u32(sm.dst[0][0]), DS_BLOCK, 1024);
     // The constant products: A = a selector (every core matrix of the 128 x 16
     // operand aliases the same 128 bytes: LBO = SBO = 0), B = the Q stage's
     // [128 queries x 16] constant tile.
@@ -482,7 +518,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
-            mma_ts(tmem + COL_DV, tmem + COL_PT + 8 * kk, nDO + os * T16 + 128 * kk, IDESC_KV,
+            mma_ts(tmem + C::COL_DV, tmem + C::COL_PT + 8 * kk, nDO + os * T16 + RB16 * kk, IDESC_KV,
                    (ci > 0 || kk > 0) ? 1u : 0u);
           tc_commit(smem_u32(&sm.p_free));
           tc_commit(smem_u32(&sm.o_empty[os]));  // the last product that reads this dO
@@ -501,8 +537,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
-            mma_ss(tmem + COL_DK, kDST + (2 * (t & 1) + (kk >> 2)) * T16 + 2 * (kk & 3),
-                   nQ + st * T16 + 128 * kk, IDESC_KV, (ci > 0 || kk > 0) ? 1u : 0u);
+            mma_ss(tmem + C::COL_DK, kDST + (2 * (t & 1) + (kk >> 2)) * DS16 + 2 * (kk & 3),
+                   nQ + st * T16 + RB16 * kk, IDESC_KV, (ci > 0 || kk > 0) ? 1u : 0u);
           tc_commit(smem_u32(&sm.q_empty[st]));
         }
         __syncwarp();
@@ -512,8 +548,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ss(tmem + COL_DQ, nDS + 2 * (t & 1) * T16 + 128 * kk, nK + slot * T16 + 128 * kk,
-                   IDESC_DQ, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + C::COL_DQ, nDS + 2 * (t & 1) * DS16 + 128 * kk,
+                   nK + slot * T16 + RB16 * kk, IDESC_DQ, kk > 0 ? 1u : 0u);
           tc_commit(smem_u32(&sm.dq_full));
           tc_commit(smem_u32(&sm.ds_free[t & 1]));
           if (ci == cur.n - 1) {
@@ -572,7 +608,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) w[i] = 0u;
         stage_acquire();
-        st_row_sw128(stage, rg, w, 0);
+        st_row_swz<C::RB>(stage, rg, w);
         stage_release();
         if (leader && key_row0 < p.n_k) {
           tma_store_3d(&tmdk, stage, 0, key_row0, item.bh);
@@ -585,28 +621,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!wait(&sm.dq_full, t & 1)) break;
         tc_fence_after();
         uint32_t a[32], b[32];
-        tmem_ld32(tmem + lane_off + COL_DQ, a);
-        tmem_ld32(tmem + lane_off + COL_DQ + 32, b);
+        tmem_ld32(tmem + lane_off + C::COL_DQ, a);
+        if constexpr (D > 32) tmem_ld32(tmem + lane_off + C::COL_DQ + 32, b);
         tmem_ld_wait(a);
-        reg_fence(b);
+        if constexpr (D > 32) reg_fence(b);
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.dq_free));
-        // two fp32 boxes of 32 columns x 64 rows per group, each added into
-        // the accumulator by one TMA reduce; rows past n_q are not touched
+        // fp32 boxes of min(d, 32) columns x 64 rows per group, each added
+        // into the accumulator by one TMA reduce; rows past n_q are not touched
         const int q_row0 = (item.qt0 + i) * BM + 64 * g;
         stage_acquire();
-        st_row_sw128(stage, rg, a, 0);
+        st_row_swz<C::QRB>(stage, rg, a);
         stage_release();
         if (leader && q_row0 < p.n_q) {
           tma_reduce_add_3d(&tmdq, stage, 0, q_row0, item.bh);
           bulk_commit_group();
         }
-        stage_acquire();
-        st_row_sw128(stage, rg, b, 0);
-        stage_release();
-        if (leader && q_row0 < p.n_q) {
-          tma_reduce_add_3d(&tmdq, stage, 32, q_row0, item.bh);
-          bulk_commit_group();
+        if constexpr (D > 32) {
+          stage_acquire();
+          st_row_swz<C::QRB>(stage, rg, b);
+          stage_release();
+          if (leader && q_row0 < p.n_q) {
+            tma_reduce_add_3d(&tmdq, stage, 32, q_row0, item.bh);
+            bulk_commit_group();
+          }
         }
       }
       if (!ok || !wait(&sm.dkv_full, it & 1)) break;
@@ -616,24 +654,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         uint32_t a[32], b[32], w[32];
-        const uint32_t col = which == 0 ? COL_DV : COL_DK;
+        const uint32_t col = which == 0 ? C::COL_DV : C::COL_DK;
         const float sc = which == 0 ? 1.f : p.scale;
         tmem_ld32(tmem + lane_off + col, a);
-        tmem_ld32(tmem + lane_off + col + 32, b);
+        if constexpr (D > 32) tmem_ld32(tmem + lane_off + col + 32, b);
         tmem_ld_wait(a);
-        reg_fence(b);
+        if constexpr (D > 32) reg_fence(b);
         if (which == 1) {
           tc_fence_before();
           mbar_arrive(smem_u32(&sm.dkv_free));
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          w[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * sc, __uint_as_float(a[2 * i + 1]) * sc);
-          w[16 + i] =
-              pack_bf16x2(__uint_as_float(b[2 * i]) * sc, __uint_as_float(b[2 * i + 1]) * sc);
+          if (i < D / 2)
+            w[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * sc, __uint_as_float(a[2 * i + 1]) * sc);
+          if constexpr (D > 32)
+            w[16 + i] =
+                pack_bf16x2(__uint_as_float(b[2 * i]) * sc, __uint_as_float(b[2 * i + 1]) * sc);
         }
         stage_acquire();
-        st_row_sw128(stage, rg, w, 0);
+        st_row_swz<C::RB>(stage, rg, w);
         stage_release();
         if (leader && key_row0 < p.n_k) {
           tma_store_3d(which == 0 ? &tmdv : &tmdk, stage, 0, key_row0, item.bh);
@@ -652,7 +692,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + COL_S + 64 * half;
     const uint32_t tDP = tmem + lane_off + COL_DP + 64 * half;
-    const uint32_t tPT = tmem + lane_off + COL_PT + 32 * half;
+    const uint32_t tPT = tmem + lane_off + C::COL_PT + 32 * half;
     const float c = p.scale_log2;
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -745,7 +785,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         // dS^T buffer t % 2 was last read by the products of tile pair t - 2
         if (!wait(&sm.ds_free[t & 1], ((t >> 1) & 1) ^ 1)) break;
-        st_row_sw128(smem_u32(sm.dst[t & 1][half]), r, e, 0);
+        st_row_swz<128>(smem_u32(sm.dst[t & 1][half]), r, e);
         fence_proxy_async_smem();
         mbar_arrive(smem_u32(&sm.ds_full));
       }
@@ -777,18 +817,20 @@ __device__ __forceinline__ uint2 split3_bf16(float x) {
   return w;
 }
 
-// Per query row (8 threads a row): D = sum_c dO_c O_c, the constant tile's
+// Per query row (d/8 threads a row, 8 elements each): D = sum_c dO_c O_c, the constant tile's
 // row for this query (b = -LSE/scale and -D, three bf16 parts each), and the
 // dQ accumulator row set to zero.  Rows n_q .. of the last query tile get zero
 // constants (their Q and dO rows are zero-filled by the tile loads, so every
 // product they enter is zero).
+template <int D>
 __global__ void __launch_bounds__(256)
     attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                         const float* __restrict__ lse, uint8_t* __restrict__ cst,
                         float* __restrict__ dq_acc, int n_q, int num_qt, float inv_scale,
                         long long rows) {
-  const long long row = static_cast<long long>(blockIdx.x) * 32 + (threadIdx.x >> 3);
-  const int sub = threadIdx.x & 7;
+  constexpr int TPR = D / 8;  // threads a row
+  const long long row = static_cast<long long>(blockIdx.x) * (256 / TPR) + threadIdx.x / TPR;
+  const int sub = threadIdx.x % TPR;
   const bool in = row < rows;
   const long long per_head = static_cast<long long>(num_qt) * BM;
   const long long bh = in ? row / per_head : 0;
@@ -812,9 +854,8 @@ __global__ void __launch_bounds__(256)
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+#pragma unroll
+  for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
   if (in && sub < 2) {
     // sub 0: columns 0-7 of this query's row (b in 0-2, -D in 3-5); sub 1:
     // columns 8-15, zero
@@ -853,29 +894,32 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-BwdLayout bwd_layout(int B, int H, int n_q) {
+BwdLayout bwd_layout(int B, int H, int n_q, int d) {
   BwdLayout l;
   const size_t bh = static_cast<size_t>(B) * H;
   l.num_qt = (n_q + BM - 1) / BM;
   l.cst_off = 0;
   l.dq_acc_off = bh * l.num_qt * CONST_TILE_BYTES;
-  l.bytes = l.dq_acc_off + bh * static_cast<size_t>(n_q) * D * 4;
+  l.bytes = l.dq_acc_off + bh * static_cast<size_t>(n_q) * d * 4;
   return l;
 }
 
-size_t bwd_tc_smem_bytes() { return sizeof(Smem) + 1024; }
+namespace {
 
-cudaError_t launch_bwd(const BwdProblem& pb, const CUtensorMap* maps, void* workspace,
-                       const LaunchCtx& ctx) {
-  const BwdLayout lay = bwd_layout(pb.B, pb.H, pb.n_q);
+template <int D>
+cudaError_t launch_bwd_d(const BwdProblem& pb, const CUtensorMap* maps, void* workspace,
+                         const LaunchCtx& ctx) {
+  static_assert(sizeof(Smem<D>) + 1024 <= 232448, "shared memory");
+  const BwdLayout lay = bwd_layout(pb.B, pb.H, pb.n_q, D);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint8_t* cst = ws + lay.cst_off;
   float* dq_acc = reinterpret_cast<float*>(ws + lay.dq_acc_off);
   const long long bh = static_cast<long long>(pb.B) * pb.H;
 
   const long long rows = bh * static_cast<long long>(lay.num_qt) * BM;
-  const long long pre_blocks = (rows + 31) / 32;
-  attn_bwd_pre_kernel<<<static_cast<unsigned>(pre_blocks), 256, 0, ctx.stream>>>(
+  constexpr int rows_per_block = 256 / (D / 8);
+  const long long pre_blocks = (rows + rows_per_block - 1) / rows_per_block;
+  attn_bwd_pre_kernel<D><<<static_cast<unsigned>(pre_blocks), 256, 0, ctx.stream>>>(
       static_cast<const __nv_bfloat16*>(pb.o), static_cast<const __nv_bfloat16*>(pb.dout), pb.lse,
       cst, dq_acc, pb.n_q, static_cast<int>(lay.num_qt), 1.f / pb.scale, rows);
   cudaError_t err = cudaGetLastError();
@@ -898,18 +942,18 @@ cudaError_t launch_bwd(const BwdProblem& pb, const CUtensorMap* maps, void* work
   p.scale = pb.scale;
   p.limit_ns = ctx.limit_ns;
   p.status = ctx.status;
-  const size_t smem = bwd_tc_smem_bytes();
+  const size_t smem = sizeof(Smem<D>) + 1024;
   const bool band = pb.mask == kMaskBand;
-  err = cudaFuncSetAttribute(band ? reinterpret_cast<const void*>(attn_bwd_tc_kernel<true>)
-                                  : reinterpret_cast<const void*>(attn_bwd_tc_kernel<false>),
+  err = cudaFuncSetAttribute(band ? reinterpret_cast<const void*>(attn_bwd_tc_kernel<true, D>)
+                                  : reinterpret_cast<const void*>(attn_bwd_tc_kernel<false, D>),
                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int grid = p.num_items < ctx.num_sms ? p.num_items : ctx.num_sms;
   if (band)
-    attn_bwd_tc_kernel<true><<<grid, NUM_THREADS, smem, ctx.stream>>>(
+    attn_bwd_tc_kernel<true, D><<<grid, NUM_THREADS, smem, ctx.stream>>>(
         maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], p);
   else
-    attn_bwd_tc_kernel<false><<<grid, NUM_THREADS, smem, ctx.stream>>>(
+    attn_bwd_tc_kernel<false, D><<<grid, NUM_THREADS, smem, ctx.stream>>>(
         maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], p);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
@@ -918,6 +962,20 @@ cudaError_t launch_bwd(const BwdProblem& pb, const CUtensorMap* maps, void* work
   attn_bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, ctx.stream>>>(
       dq_acc, static_cast<__nv_bfloat16*>(pb.dq), pb.scale, n8);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_head_size_ok(int d) { return d == 16 || d == 32 || d == 64; }
+
+cudaError_t launch_bwd(const BwdProblem& pb, const CUtensorMap* maps, void* workspace,
+                       const LaunchCtx& ctx) {
+  switch (pb.d) {
+    case 16: return launch_bwd_d<16>(pb, maps, workspace, ctx);
+    case 32: return launch_bwd_d<32>(pb, maps, workspace, ctx);
+    case 64: return launch_bwd_d<64>(pb, maps, workspace, ctx);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace attn

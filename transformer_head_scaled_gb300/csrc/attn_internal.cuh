@@ -74,18 +74,18 @@ DecodePlan decode_plan(int B, int H, int n_q, int L_max, int num_sms);
 cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap* maps, const DecodePlan& plan,
                           float* workspace, const LaunchCtx& ctx);
 
-// Backward (d = 64, bf16): gradients of the forward above.
+// Backward (d = 16, 32 or 64; bf16): gradients of the forward above.
 struct BwdProblem {
-  const void* q;     // bf16 [B, H, n_q, 64]
-  const void* k;     // bf16 [B, H, n_k, 64]
+  const void* q;     // bf16 [B, H, n_q, d]
+  const void* k;     // bf16 [B, H, n_k, d]
   const void* v;
-  const void* o;     // the forward's output, bf16 [B, H, n_q, 64]
-  const void* dout;  // dLoss/dO, bf16 [B, H, n_q, 64]
+  const void* o;     // the forward's output, bf16 [B, H, n_q, d]
+  const void* dout;  // dLoss/dO, bf16 [B, H, n_q, d]
   const float* lse;  // the forward's log-sum-exp [B, H, n_q]
   void* dq;          // bf16 outputs, shaped like q, k, v
   void* dk;
   void* dv;
-  int B, H, n_q, n_k;
+  int B, H, n_q, n_k, d;
   float scale;
   int mask;
   const int* key_lens;
@@ -94,16 +94,16 @@ struct BwdProblem {
 
 // Workspace of the backward: the per-query constant tiles (one [128 x 16]
 // bf16 tile of 4 KB per 128-query tile and head), then the fp32 dQ
-// accumulator [B, H, n_q, 64].
+// accumulator [B, H, n_q, d].
 struct BwdLayout {
   size_t num_qt, cst_off, dq_acc_off, bytes;
 };
-BwdLayout bwd_layout(int B, int H, int n_q);
-size_t bwd_tc_smem_bytes();
-// maps: Q, K, V, dO as 3-D (64, n, B*H) bf16 with a (64, 128, 1) box; dK, dV
-// the same with a (64, 64, 1) box; the dQ accumulator as 3-D (64, n_q, B*H)
-// fp32 with a (32, 64, 1) box; all with 128-byte swizzle.  Three launches
-// (preprocess, main, dQ convert).
+BwdLayout bwd_layout(int B, int H, int n_q, int d);
+bool bwd_head_size_ok(int d);
+// maps: Q, K, V, dO as 3-D (d, n, B*H) bf16 with a (d, 128, 1) box; dK, dV
+// the same with a (d, 64, 1) box; the dQ accumulator as 3-D (d, n_q, B*H)
+// fp32 with a (min(d, 32), 64, 1) box; each in the swizzle of its box's row
+// bytes.  Three launches (preprocess, main, dQ convert).
 cudaError_t launch_bwd(const BwdProblem& pb, const CUtensorMap* maps, void* workspace,
                        const LaunchCtx& ctx);
 

@@ -117,6 +117,10 @@ WORKLOADS = {
     "big_window_bwd": Workload("big_window_bwd", 8, 16, 4096, 4096, 64, MASK_BAND, "bf16",
                                win_left=256, win_right=256, kind="bwd",
                                note="backward of restricted self-attention, window of 513"),
+    "base_h16_d32_bwd": Workload("base_h16_d32_bwd", 64, 16, 512, 512, 32, MASK_NONE, "bf16",
+                                 kind="bwd", note="backward, base encoder, 16 heads of 32"),
+    "base_h32_d16_bwd": Workload("base_h32_d16_bwd", 64, 32, 512, 512, 16, MASK_NONE, "bf16",
+                                 kind="bwd", note="backward, base encoder, 32 heads of 16"),
 }
 
 
