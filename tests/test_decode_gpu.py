@@ -118,3 +118,21 @@ def test_decode_workloads_full(name):
     o, lse = binding.attn_decode(q, k, v, kl, scale=w.scale)
     binding.check()
     _check(o, lse, q, k, v, kl, w.scale)
+
+
+@pytest.mark.parametrize("B,h,L_max", [
+    (600, 4, 300),    # several units per CTA, ordered longest first
+    (1100, 1, 64),    # more (batch entry, split) pairs than the ordering takes: index order
+    (1000, 16, 32),   # more units per CTA than its schedule holds: index order
+    (40, 2, 3000),    # split caches: (batch entry, split) pairs ordered by key count
+])
+def test_decode_many_units_every_row(B, h, L_max):
+    """Every unit is processed exactly once whatever order the CTAs take them in:
+    random lengths (zeros and full caches included), every output row checked."""
+    rng = np.random.default_rng(B * 7 + h)
+    lens = rng.integers(0, L_max + 1, size=B)
+    lens[:3] = [0, L_max, 1]
+    w, q, k, v, kl = _case(B, h, 1, L_max, lens.tolist(), seed=3)
+    o, lse = binding.attn_decode(q, k, v, kl, scale=w.scale)
+    binding.check()
+    _check(o, lse, q, k, v, kl, w.scale)

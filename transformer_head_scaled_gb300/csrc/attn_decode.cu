@@ -37,6 +37,14 @@ constexpr uint32_t TILE_BYTES = KT * DK * 2;  // 16 KB
 constexpr int TAIL = 32;                        // keys per box of a partial last tile
 constexpr uint32_t TAIL_BYTES = TAIL * DK * 2;  // 4 KB (a multiple of the 1 KB swizzle atom)
 constexpr float LN2 = 0.693147180559945309f;
+// Longest-first schedule: when the caches have lengths and there are at most
+// SORT_MAX (batch entry, split) pairs, the CTAs take the work units in order
+// of decreasing key count, dealt out in snake order (CTA 0..G-1, then
+// G-1..0, ...), instead of round-robin by index; each CTA holds at most
+// SCHED_MAX units of its own.
+constexpr int SORT_MAX = 1024;
+constexpr int SCHED_MAX = 32;
+constexpr int NBUCKET = 64;  // key-count classes of that ordering
 
 struct __align__(1024) DecSmem {
   uint8_t k[DSTAGES][TILE_BYTES];
@@ -44,8 +52,14 @@ struct __align__(1024) DecSmem {
   union {
     float q[kDecodeMaxQueries][DK];                // queries, pre-scaled by scale*log2(e)
     float red[NWARPS][kDecodeMaxQueries][DK + 2];  // per-warp partials, after the tiles
+    struct {
+      int count[NBUCKET];  // (batch entry, split) pairs per key-count class
+      int first[NBUCKET];  // sorted position of each class's first pair
+    } sort;                // before the first unit
   };
   uint64_t full[DSTAGES], empty[DSTAGES];
+  int sched[SCHED_MAX];  // this CTA's units, in processing order
+  int nsched;
   int abort;
 };
 
@@ -107,18 +121,98 @@ __global__ void __launch_bounds__(THREADS, 3)
     sm.abort = 0;
     fence_mbar_init();
   }
+
+  // ---- this CTA's units.  A unit is one (batch entry, split) pair of one
+  // head; the pairs are the sort keys (every head of a pair has the same
+  // keys), the heads of a pair stay adjacent in the order.
+  const int G = gridDim.x;
+  const int pairs = (p.BH / p.H) * p.splits;
+  const bool sorted =
+      p.cache_lens != nullptr && pairs <= SORT_MAX && (units + G - 1) / G <= SCHED_MAX;
+  if (sorted) {
+    const int maxk = max(1, min(p.chunk, p.L_max));
+    auto bucket_of = [&](int e) {  // key-count class of pair e (0: no key)
+      const int L = min(max(__ldg(p.cache_lens + e / p.splits), 0), p.L_max);
+      const int begin = (e % p.splits) * p.chunk;
+      const int keys = min(L, begin + p.chunk) - begin;
+      return keys <= 0 ? 0 : 1 + min(NBUCKET - 2, ((keys - 1) * (NBUCKET - 1)) / maxk);
+    };
+    for (int i = threadIdx.x; i < NBUCKET; i += THREADS) sm.sort.count[i] = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < pairs; e += THREADS) atomicAdd(&sm.sort.count[bucket_of(e)], 1);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int acc = 0;  // classes in decreasing order of key count
+      for (int k = NBUCKET - 1; k >= 0; --k) {
+        sm.sort.first[k] = acc;
+        acc += sm.sort.count[k];
+      }
+    }
+    __syncthreads();
+    // unit position i*G + c (i even) or i*G + G-1-c (i odd) of the sorted
+    // order; inside a class the pairs keep their index order
+    int n_mine = 0;
+    for (int i = 0; i < SCHED_MAX; ++i) {
+      const int pos = i * G + ((i & 1) ? G - 1 - static_cast<int>(blockIdx.x) : blockIdx.x);
+      if (pos >= units) break;
+      n_mine = i + 1;
+    }
+    for (int i = warp; i < n_mine; i += NWARPS) {
+      const int pos = i * G + ((i & 1) ? G - 1 - static_cast<int>(blockIdx.x) : blockIdx.x);
+      const int pq = pos / p.H, hh = pos % p.H;  // sorted pair position, head
+      int k = 0;
+#pragma unroll 1
+      for (int k0 = 0; k0 < NBUCKET; k0 += 32) {
+        const int kk = k0 + lane;
+        const bool hit = sm.sort.count[kk] > 0 && sm.sort.first[kk] <= pq &&
+                         pq < sm.sort.first[kk] + sm.sort.count[kk];
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (m != 0u) {
+          k = k0 + __ffs(m) - 1;
+          break;
+        }
+      }
+      int rank = pq - sm.sort.first[k];  // among the pairs of class k, by index
+      int e_at = 0;
+#pragma unroll 1
+      for (int e0 = 0; e0 < pairs; e0 += 32) {
+        const int e = e0 + lane;
+        unsigned m = __ballot_sync(0xffffffffu, e < pairs && bucket_of(e) == k);
+        const int cnt = __popc(m);
+        if (rank < cnt) {
+          for (int z = 0; z < rank; ++z) m &= m - 1u;
+          e_at = e0 + __ffs(m) - 1;
+          break;
+        }
+        rank -= cnt;
+      }
+      if (lane == 0) {
+        const int b = e_at / p.splits, sp = e_at % p.splits;
+        sm.sched[i] = (b * p.H + hh) * p.splits + sp;
+      }
+    }
+    if (threadIdx.x == 0) sm.nsched = n_mine;
+  }
   __syncthreads();
+  const int n_units = sorted ? sm.nsched
+                             : (static_cast<int>(blockIdx.x) < units
+                                    ? (units - 1 - static_cast<int>(blockIdx.x)) / G + 1
+                                    : 0);
+  auto unit_at = [&](int i) {  // this CTA's i-th unit (units: none left)
+    if (i >= n_units) return units;
+    return sorted ? sm.sched[i] : static_cast<int>(blockIdx.x) + i * G;
+  };
   const volatile int* abort = &sm.abort;
   const bool producer = threadIdx.x == 0;
 
   // ---- producer state (thread 0): the next (unit, tile) to load
-  int pu = blockIdx.x, pt = 0, pbh = 0, pbegin = 0, pend = 0;
+  int pi = 0, pu = unit_at(0), pt = 0, pbh = 0, pbegin = 0, pend = 0;
   if (producer && pu < units) unit_keys(pu, pbh, pbegin, pend);
   uint32_t issued = 0;
   bool pok = true;
   auto produce_one = [&]() {
     while (pu < units && pbegin + pt * KT >= pend) {
-      pu += gridDim.x;
+      pu = unit_at(++pi);
       pt = 0;
       if (pu < units) unit_keys(pu, pbh, pbegin, pend);
     }
@@ -169,12 +263,13 @@ __global__ void __launch_bounds__(THREADS, 3)
     }
   };
   float qv[QPT];
-  load_q(blockIdx.x, qv);
+  load_q(unit_at(0), qv);
 
   uint32_t consumed = 0;
   bool ok = true;
   const int r = warp * 32 + lane;  // this lane's key row inside a tile
-  for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+  for (int ui = 0; ui < n_units && ok; ++ui) {
+    const int u = unit_at(ui);
     int bh, begin, end;
     unit_keys(u, bh, begin, end);
     const int ntiles = end > begin ? (end - begin + KT - 1) / KT : 0;
@@ -185,7 +280,7 @@ __global__ void __launch_bounds__(THREADS, 3)
       if (e < NQ * DK) sm.q[e / DK][e % DK] = qv[i] * p.scale_log2;
     }
     __syncthreads();
-    load_q(u + gridDim.x, qv);  // the next unit's queries, consumed after this unit
+    load_q(unit_at(ui + 1), qv);  // the next unit's queries, consumed after this unit
 
     float m[NQ], l[NQ], o0[NQ], o1[NQ];  // this warp's running state per query
 #pragma unroll
