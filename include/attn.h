@@ -224,6 +224,25 @@ int attn_bwd_window(const void* q, const void* k, const void* v, const void* o, 
                     int n_k, int d_k, float scale, int window_left, int window_right,
                     void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
+/*
+ * attn_bwd_strided -- attn_bwd (or attn_bwd_window) on tensors of any row,
+ * head and batch strides, the gradient of attn_fwd_strided: element
+ * (b, hh, i, t) of each tensor X is  x[b*s[0] + hh*s[1] + i*s[2] + t].
+ * strides is a host array of 24 element counts, three (b, h, row) per tensor
+ * in the order q, k, v, o, dout, dq, dk, dv; each > 0 and a multiple of 8 (16
+ * bytes); d is contiguous.  dq, dk, dv are written through their strides (for
+ * instance into one packed [B, n, 3, h, d] gradient buffer) and must not
+ * overlap the inputs; lse stays contiguous [B, h, n_q].  mask_kind: any
+ * attn_mask_kind; ATTN_MASK_WINDOW uses window_left / window_right as
+ * attn_bwd_window does (both ignored otherwise).  Other arguments as
+ * attn_bwd (d_k in {16, 32, 64}; the same workspace size).
+ */
+int attn_bwd_strided(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int h, int n_q,
+                     int n_k, int d_k, const int64_t* strides, float scale, int mask_kind,
+                     const int* key_lens, int window_left, int window_right, void* workspace,
+                     size_t workspace_bytes, struct CUstream_st* stream);
+
 /* Scratch bytes attn_bwd needs for these sizes (0 for unsupported sizes). */
 size_t attn_bwd_workspace_bytes(int B, int h, int n_q, int d_k);
 

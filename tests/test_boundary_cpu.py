@@ -200,3 +200,26 @@ def test_bwd_window_arguments_rejected_on_host(lib):
     # attn_bwd itself takes no window
     assert binding.attn_bwd_raw(A, A, A, A, A, A, A, A, A, 1, 1, 8, 8, 64, 0.125, 3, None, A,
                                 1 << 30, None) == INV
+
+
+def test_bwd_strided_arguments_rejected_on_host(lib):
+    good = [(8 * 64 * 8, 64, 8 * 64)] * 8   # [B, n, h, d] strides of a [B, h, n, d] view
+
+    def call(strides=good, mask=0, lens=None, left=0, right=0, d=64, q=A, ws_bytes=1 << 30):
+        return binding.attn_bwd_strided_raw(q, A, A, A, A, A, A, A, A, 1, 8, 8, 8, d, strides,
+                                            0.125, mask, lens, left, right, A, ws_bytes, None)
+    INV = binding.ATTN_ERR_INVALID_ARG
+    for i in range(8):   # every tensor's strides are checked: 16-byte multiples, positive
+        bad = list(good)
+        bad[i] = (8 * 64 * 8, 64, 8 * 64 + 4)
+        assert call(strides=bad) == INV, i
+        bad[i] = (0, 64, 512)
+        assert call(strides=bad) == INV, i
+    assert call(mask=3, left=-1) == INV
+    assert call(mask=4) == INV
+    assert call(mask=2, lens=None) == INV
+    assert call(q=None) == INV
+    assert call(ws_bytes=16) == INV
+    assert call(d=128) == binding.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_bwd_strided(A, A, A, A, A, A, A, A, A, 1, 8, 8, 8, 64, None, 0.125, 0, None,
+                                0, 0, A, 1 << 30, None) == INV   # no stride array

@@ -30,7 +30,8 @@ DECODE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 # Every entry point declared in include/attn.h.
 EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_fwd_window", "attn_fwd_strided", "attn_decode", "attn_decode_workspace_bytes",
-           "attn_decode_noalloc", "attn_bwd", "attn_bwd_window", "attn_bwd_workspace_bytes",
+           "attn_decode_noalloc", "attn_bwd", "attn_bwd_window", "attn_bwd_strided",
+           "attn_bwd_workspace_bytes",
            "attn_check", "attn_status_string",
            "attn_last_cuda_error", "attn_set_wait_limit_ns", "attn_launch_count",
            "attn_diag_tile", "attn_diag_wait_timeout")
@@ -80,6 +81,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         lib.attn_bwd.restype = i32
         lib.attn_bwd.argtypes = [vp] * 9 + [i32] * 5 + [f32, i32, vp, vp, ctypes.c_size_t, vp]
+        lib.attn_bwd_strided.restype = i32
+        lib.attn_bwd_strided.argtypes = [vp] * 9 + [i32] * 5 + [vp, f32, i32, vp, i32, i32, vp,
+                                                                 ctypes.c_size_t, vp]
         lib.attn_bwd_window.restype = i32
         lib.attn_bwd_window.argtypes = [vp] * 9 + [i32] * 5 + [f32, i32, i32, vp, ctypes.c_size_t,
                                                                 vp]
@@ -329,6 +333,67 @@ def attn_bwd_window_raw(q_ptr, k_ptr, v_ptr, o_ptr, dout_ptr, lse_ptr, dq_ptr, d
     return load().attn_bwd_window(q_ptr, k_ptr, v_ptr, o_ptr, dout_ptr, lse_ptr, dq_ptr, dk_ptr,
                                   dv_ptr, B, h, n_q, n_k, d, float(scale), int(left), int(right),
                                   ws_ptr, int(ws_bytes), stream_ptr)
+
+
+def attn_bwd_strided_raw(q_ptr, k_ptr, v_ptr, o_ptr, dout_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr, B,
+                         h, n_q, n_k, d, strides, scale, mask_kind, lens_ptr, left, right, ws_ptr,
+                         ws_bytes, stream_ptr) -> int:
+    """The C call itself; ``strides`` = eight (b, h, n) element-stride triples for q, k, v, o,
+    dout, dq, dk, dv."""
+    flat = (ctypes.c_int64 * 24)(*[int(x) for st in strides for x in st])
+    return load().attn_bwd_strided(q_ptr, k_ptr, v_ptr, o_ptr, dout_ptr, lse_ptr, dq_ptr, dk_ptr,
+                                   dv_ptr, B, h, n_q, n_k, d, ctypes.cast(flat, ctypes.c_void_p),
+                                   float(scale), int(mask_kind), lens_ptr, int(left), int(right),
+                                   ws_ptr, int(ws_bytes), stream_ptr)
+
+
+def attn_bwd_strided(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                     lse: torch.Tensor, dout: torch.Tensor, dq: torch.Tensor, dk: torch.Tensor,
+                     dv: torch.Tensor, scale: float | None = None, mask: int = MASK_NONE,
+                     key_lens: torch.Tensor | None = None,
+                     window: tuple[int, int] | None = None,
+                     workspace: torch.Tensor | None = None, stream=None):
+    """attn_bwd on [B, h, n, d] bf16 views with any strides over the first three
+    dimensions and a contiguous last one; the gradients are written into the
+    given dq, dk, dv views (e.g. slices of one packed gradient buffer).
+    ``window=(left, right)`` differentiates restricted self-attention."""
+    for t in (q, k, v, o, dout, dq, dk, dv):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or t.stride(-1) != 1:
+            raise ValueError("tensors must be bf16 CUDA [B, h, n, d] views with unit last stride")
+    B, h, n_q, d = q.shape
+    n_k = k.shape[2]
+    for t in (k, v, dk, dv):
+        if tuple(t.shape) != (B, h, n_k, d):
+            raise ValueError("k, v, dk, dv must be [B, h, n_k, d] with q's B, h, d")
+    for t in (o, dout, dq):
+        if tuple(t.shape) != (B, h, n_q, d):
+            raise ValueError("o, dout, dq must be shaped like q")
+    if (lse is None or not lse.is_cuda or lse.dtype != torch.float32
+            or tuple(lse.shape) != (B, h, n_q) or not lse.is_contiguous()):
+        raise ValueError("lse must be the forward's contiguous float32 [B, h, n_q] CUDA tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    kl, left, right = None, 0, 0
+    if window is not None:
+        mask, (left, right) = MASK_WINDOW, window
+    if mask == MASK_KEY_PADDING:
+        if key_lens is None:
+            raise ValueError("key padding needs key_lens")
+        kl = key_lens
+        if kl.dtype != torch.int32 or not kl.is_cuda or kl.numel() != B or not kl.is_contiguous():
+            raise ValueError("key_lens must be a contiguous int32 CUDA tensor of B entries")
+    need = bwd_workspace_bytes(B, h, n_q, d)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    strides = [t.stride()[:3] for t in (q, k, v, o, dout, dq, dk, dv)]
+    rc = attn_bwd_strided_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                              _ptr(dk), _ptr(dv), B, h, n_q, n_k, d, strides, scale, int(mask),
+                              _ptr(kl), left, right, _ptr(workspace), ws_bytes,
+                              _stream_ptr(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd_strided")
+    return dq, dk, dv
 
 
 def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,

@@ -150,9 +150,7 @@ int encode_3d_f32(CUtensorMap* map, const void* base, int d, int n, long long bh
 bool tc_head_size(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
 // Element strides of a [B, h, n, d] tensor view (d contiguous).
-struct Strides {
-  long long b, h, n;
-};
+using Strides = RowStrides;
 
 Strides bhsd(int h, int n, int d) {
   return Strides{static_cast<long long>(h) * n * d, static_cast<long long>(n) * d, d};
@@ -436,11 +434,13 @@ size_t attn_bwd_workspace_bytes(int B, int h, int n_q, int d_k) {
 
 namespace attn {
 namespace {
+// st: strides of q, k, v, o, dout, dq, dk, dv, or null for contiguous
+// [B, h, n, d] tensors.
 static int bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout,
                     const float* lse, void* dq, void* dk, void* dv, int B, int h, int n_q,
-                    int n_k, int d_k, float scale, int mask_kind, const int* key_lens,
-                    int window_left, int window_right, void* workspace, size_t workspace_bytes,
-                    struct CUstream_st* stream) {
+                    int n_k, int d_k, const Strides* st, float scale, int mask_kind,
+                    const int* key_lens, int window_left, int window_right, void* workspace,
+                    size_t workspace_bytes, struct CUstream_st* stream) {
   const bool window = mask_kind == kMaskBand;
   int rc = check_common(q, k, v, o, lse, B, h, n_q, n_k, d_k, scale,
                         window ? ATTN_MASK_NONE : mask_kind, key_lens, 2);
@@ -455,13 +455,17 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di)) != ATTN_OK) return rc;
   const long long bh = static_cast<long long>(B) * h;
+  const Strides rq = bhsd(h, n_q, d_k), rk = bhsd(h, n_k, d_k);
+  const Strides sq = st ? st[0] : rq, sk = st ? st[1] : rk, sv = st ? st[2] : rk,
+                so = st ? st[3] : rq, sdo = st ? st[4] : rq, sdq = st ? st[5] : rq,
+                sdk = st ? st[6] : rk, sdv = st ? st[7] : rk;
   CUtensorMap maps[7];
-  if ((rc = encode_3d(&maps[0], q, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&maps[1], k, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&maps[2], v, d_k, n_k, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&maps[3], dout, d_k, n_q, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&maps[4], dk, d_k, n_k, bh, 64)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&maps[5], dv, d_k, n_k, bh, 64)) != ATTN_OK) return rc;
+  if ((rc = encode_4d(&maps[0], q, d_k, n_q, h, B, sq, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_4d(&maps[1], k, d_k, n_k, h, B, sk, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_4d(&maps[2], v, d_k, n_k, h, B, sv, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_4d(&maps[3], dout, d_k, n_q, h, B, sdo, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_4d(&maps[4], dk, d_k, n_k, h, B, sdk, 64)) != ATTN_OK) return rc;
+  if ((rc = encode_4d(&maps[5], dv, d_k, n_k, h, B, sdv, 64)) != ATTN_OK) return rc;
   if ((rc = encode_3d_f32(&maps[6], static_cast<uint8_t*>(workspace) + lay.dq_acc_off, d_k, n_q,
                           bh)) != ATTN_OK)
     return rc;
@@ -469,7 +473,7 @@ static int bwd_impl(const void* q, const void* k, const void* v, const void* o, 
   BwdProblem pb{q, k, v, o, dout, lse, dq, dk, dv, B, h, n_q, n_k, d_k, scale, mask_kind,
                 mask_kind == ATTN_MASK_KEY_PADDING ? key_lens : nullptr,
                 window_left < reach ? window_left : reach,
-                window_right < reach ? window_right : reach};
+                window_right < reach ? window_right : reach, so, sdo, sdq};
   cudaError_t e = launch_bwd(pb, maps, workspace, make_ctx(*di, stream));
   if (e != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(3);
@@ -485,8 +489,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              int d_k, float scale, int mask_kind, const int* key_lens, void* workspace,
              size_t workspace_bytes, struct CUstream_st* stream) {
   if (mask_kind == ATTN_MASK_WINDOW) return ATTN_ERR_INVALID_ARG;  // attn_bwd_window
-  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, h, n_q, n_k, d_k, scale, mask_kind,
-                  key_lens, 0, 0, workspace, workspace_bytes, stream);
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, h, n_q, n_k, d_k, nullptr, scale,
+                  mask_kind, key_lens, 0, 0, workspace, workspace_bytes, stream);
 }
 
 int attn_bwd_window(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -494,8 +498,31 @@ int attn_bwd_window(const void* q, const void* k, const void* v, const void* o, 
                     int n_k, int d_k, float scale, int window_left, int window_right,
                     void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
   if (window_left < 0 || window_right < 0) return ATTN_ERR_INVALID_ARG;
-  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, h, n_q, n_k, d_k, scale, kMaskBand,
-                  nullptr, window_left, window_right, workspace, workspace_bytes, stream);
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, h, n_q, n_k, d_k, nullptr, scale,
+                  kMaskBand, nullptr, window_left, window_right, workspace, workspace_bytes,
+                  stream);
+}
+
+int attn_bwd_strided(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int h, int n_q,
+                     int n_k, int d_k, const int64_t* strides, float scale, int mask_kind,
+                     const int* key_lens, int window_left, int window_right, void* workspace,
+                     size_t workspace_bytes, struct CUstream_st* stream) {
+  if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_WINDOW) return ATTN_ERR_INVALID_ARG;
+  if (mask_kind == ATTN_MASK_WINDOW && (window_left < 0 || window_right < 0))
+    return ATTN_ERR_INVALID_ARG;
+  if (strides == nullptr) return ATTN_ERR_INVALID_ARG;
+  Strides st[8];
+  for (int i = 0; i < 8; ++i) {
+    st[i] = Strides{strides[3 * i], strides[3 * i + 1], strides[3 * i + 2]};
+    if (!stride_ok(st[i].b) || !stride_ok(st[i].h) || !stride_ok(st[i].n))
+      return ATTN_ERR_INVALID_ARG;
+  }
+  const bool window = mask_kind == ATTN_MASK_WINDOW;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, h, n_q, n_k, d_k, st, scale,
+                  window ? static_cast<int>(kMaskBand) : mask_kind, window ? nullptr : key_lens,
+                  window ? window_left : 0, window ? window_right : 0, workspace,
+                  workspace_bytes, stream);
 }
 
 int attn_check(struct CUstream_st* stream) {

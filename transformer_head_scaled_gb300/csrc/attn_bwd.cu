@@ -365,8 +365,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ok = mbar_wait(smem_u32(&sm.k_empty[slot]), ((it >> 1) & 1) ^ 1, p.limit_ns, abort);
         if (!ok) break;
         mbar_arrive_expect_tx(smem_u32(&sm.k_full[slot]), C::TILE);
-        tma_load_3d(smem_u32(sm.k[slot]), &tmk, smem_u32(&sm.k_full[slot]), 0, item.kt * BN,
-                    item.bh);
+        tma_load_4d(smem_u32(sm.k[slot]), &tmk, smem_u32(&sm.k_full[slot]), 0, item.kt * BN,
+                    item.bh % p.H, item.bh / p.H);
         ++it;
         for (int i = 0; i < item.n && ok; ++i) {
           const int qt = item.qt0 + i;
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!ok) break;
           const uint32_t qb = smem_u32(&sm.q_full[st]);
           mbar_arrive_expect_tx(qb, C::TILE + CONST_TILE_BYTES);
-          tma_load_3d(smem_u32(sm.q[st]), &tmq, qb, 0, qt * BM, item.bh);
+          tma_load_4d(smem_u32(sm.q[st]), &tmq, qb, 0, qt * BM, item.bh % p.H, item.bh / p.H);
           const size_t tile = static_cast<size_t>(item.bh) * p.num_qt + qt;
           bulk_load(smem_u32(sm.cst[st]), p.cst + tile * CONST_TILE_BYTES, CONST_TILE_BYTES, qb);
           ++nq;
@@ -384,7 +384,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = mbar_wait(smem_u32(&sm.v_empty), (nv & 1) ^ 1, p.limit_ns, abort);
             if (!ok) break;
             mbar_arrive_expect_tx(smem_u32(&sm.v_full), C::TILE);
-            tma_load_3d(smem_u32(sm.v), &tmv, smem_u32(&sm.v_full), 0, item.kt * BN, item.bh);
+            tma_load_4d(smem_u32(sm.v), &tmv, smem_u32(&sm.v_full), 0, item.kt * BN,
+                        item.bh % p.H, item.bh / p.H);
             ++nv;
           }
           const uint32_t os = no % OSTAGES;
@@ -392,7 +393,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!ok) break;
           const uint32_t ob = smem_u32(&sm.o_full[os]);
           mbar_arrive_expect_tx(ob, C::TILE);
-          tma_load_3d(smem_u32(sm.dout[os]), &tmdo, ob, 0, qt * BM, item.bh);
+          tma_load_4d(smem_u32(sm.dout[os]), &tmdo, ob, 0, qt * BM, item.bh % p.H,
+                      item.bh / p.H);
           ++no;
         }
       }
@@ -611,8 +613,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         st_row_swz<C::RB>(stage, rg, w);
         stage_release();
         if (leader && key_row0 < p.n_k) {
-          tma_store_3d(&tmdk, stage, 0, key_row0, item.bh);
-          tma_store_3d(&tmdv, stage, 0, key_row0, item.bh);
+          tma_store_4d(&tmdk, stage, 0, key_row0, item.bh % p.H, item.bh / p.H);
+          tma_store_4d(&tmdv, stage, 0, key_row0, item.bh % p.H, item.bh / p.H);
           bulk_commit_group();
         }
         continue;
@@ -676,7 +678,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         st_row_swz<C::RB>(stage, rg, w);
         stage_release();
         if (leader && key_row0 < p.n_k) {
-          tma_store_3d(which == 0 ? &tmdv : &tmdk, stage, 0, key_row0, item.bh);
+          tma_store_4d(which == 0 ? &tmdv : &tmdk, stage, 0, key_row0, item.bh % p.H,
+                       item.bh / p.H);
           bulk_commit_group();
         }
       }
@@ -826,8 +829,8 @@ template <int D>
 __global__ void __launch_bounds__(256)
     attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                         const float* __restrict__ lse, uint8_t* __restrict__ cst,
-                        float* __restrict__ dq_acc, int n_q, int num_qt, float inv_scale,
-                        long long rows) {
+                        float* __restrict__ dq_acc, int H, int n_q, int num_qt, float inv_scale,
+                        long long rows, RowStrides so, RowStrides sdo) {
   constexpr int TPR = D / 8;  // threads a row
   const long long row = static_cast<long long>(blockIdx.x) * (256 / TPR) + threadIdx.x / TPR;
   const int sub = threadIdx.x % TPR;
@@ -836,11 +839,13 @@ __global__ void __launch_bounds__(256)
   const long long bh = in ? row / per_head : 0;
   const int i = in ? static_cast<int>(row - bh * per_head) : 0;  // query index
   const bool valid = in && i < n_q;
-  const size_t src = (static_cast<size_t>(bh) * n_q + i) * D + sub * 8;
+  const size_t src = (static_cast<size_t>(bh) * n_q + i) * D + sub * 8;  // accumulator row
+  const long long bb = bh / H, hh = bh % H;
   float acc = 0.f;
   if (valid) {
-    const uint4 a = *reinterpret_cast<const uint4*>(dout + src);
-    const uint4 b = *reinterpret_cast<const uint4*>(o + src);
+    const uint4 a =
+        *reinterpret_cast<const uint4*>(dout + bb * sdo.b + hh * sdo.h + i * sdo.n + sub * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(o + bb * so.b + hh * so.h + i * so.n + sub * 8);
     const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
     const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
@@ -876,12 +881,17 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// dQ = scale * accumulator, rounded to bf16; 8 elements a thread.
+// dQ = scale * accumulator, rounded to bf16, written through dq's strides;
+// 8 elements a thread (d8 = d / 8 threads a row).
 __global__ void __launch_bounds__(256)
     attn_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
-                       float scale, long long n8) {
+                       float scale, long long n8, int d8, int H, int n_q, RowStrides sdq) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n8) return;
+  const long long r = i / d8;  // row (b * H + hh) * n_q + qi of the accumulator
+  const long long bh = r / n_q;
+  const long long dst =
+      (bh / H) * sdq.b + (bh % H) * sdq.h + (r - bh * n_q) * sdq.n + (i - r * d8) * 8;
   const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
   const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
   uint4 out;
@@ -889,7 +899,7 @@ __global__ void __launch_bounds__(256)
   out.y = pack_bf16x2(a.z * scale, a.w * scale);
   out.z = pack_bf16x2(b.x * scale, b.y * scale);
   out.w = pack_bf16x2(b.z * scale, b.w * scale);
-  reinterpret_cast<uint4*>(dq)[i] = out;
+  *reinterpret_cast<uint4*>(dq + dst) = out;
 }
 
 }  // namespace
@@ -921,7 +931,8 @@ cudaError_t launch_bwd_d(const BwdProblem& pb, const CUtensorMap* maps, void* wo
   const long long pre_blocks = (rows + rows_per_block - 1) / rows_per_block;
   attn_bwd_pre_kernel<D><<<static_cast<unsigned>(pre_blocks), 256, 0, ctx.stream>>>(
       static_cast<const __nv_bfloat16*>(pb.o), static_cast<const __nv_bfloat16*>(pb.dout), pb.lse,
-      cst, dq_acc, pb.n_q, static_cast<int>(lay.num_qt), 1.f / pb.scale, rows);
+      cst, dq_acc, pb.H, pb.n_q, static_cast<int>(lay.num_qt), 1.f / pb.scale, rows, pb.so,
+      pb.sdo);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
 
@@ -960,7 +971,7 @@ cudaError_t launch_bwd_d(const BwdProblem& pb, const CUtensorMap* maps, void* wo
 
   const long long n8 = bh * pb.n_q * (D / 8);
   attn_bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, ctx.stream>>>(
-      dq_acc, static_cast<__nv_bfloat16*>(pb.dq), pb.scale, n8);
+      dq_acc, static_cast<__nv_bfloat16*>(pb.dq), pb.scale, n8, D / 8, pb.H, pb.n_q, pb.sdq);
   return cudaGetLastError();
 }
 

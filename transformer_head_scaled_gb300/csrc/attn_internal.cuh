@@ -74,6 +74,12 @@ DecodePlan decode_plan(int B, int H, int n_q, int L_max, int num_sms);
 cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap* maps, const DecodePlan& plan,
                           float* workspace, const LaunchCtx& ctx);
 
+// Element strides of a [B, H, n, d] view across batch entries, heads and rows
+// (d contiguous).
+struct RowStrides {
+  long long b, h, n;
+};
+
 // Backward (d = 16, 32 or 64; bf16): gradients of the forward above.
 struct BwdProblem {
   const void* q;     // bf16 [B, H, n_q, d]
@@ -90,6 +96,7 @@ struct BwdProblem {
   int mask;
   const int* key_lens;
   int win_left, win_right;  // kMaskBand: query i sees keys i - win_left .. i + win_right
+  RowStrides so, sdo, sdq;  // strides of o, dout (read with plain loads) and dq (written so)
 };
 
 // Workspace of the backward: the per-query constant tiles (one [128 x 16]
@@ -100,8 +107,8 @@ struct BwdLayout {
 };
 BwdLayout bwd_layout(int B, int H, int n_q, int d);
 bool bwd_head_size_ok(int d);
-// maps: Q, K, V, dO as 3-D (d, n, B*H) bf16 with a (d, 128, 1) box; dK, dV
-// the same with a (d, 64, 1) box; the dQ accumulator as 3-D (d, n_q, B*H)
+// maps: Q, K, V, dO as 4-D (d, n, H, B) bf16 with a (d, 128, 1, 1) box; dK,
+// dV the same with a (d, 64, 1, 1) box (any strides); the dQ accumulator as 3-D (d, n_q, B*H)
 // fp32 with a (min(d, 32), 64, 1) box; each in the swizzle of its box's row
 // bytes.  Three launches (preprocess, main, dQ convert).
 cudaError_t launch_bwd(const BwdProblem& pb, const CUtensorMap* maps, void* workspace,
