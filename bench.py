@@ -508,8 +508,24 @@ def run_e2e(args, w, q, k, v, kl, dev, stream, f32):
     ws_bytes = (binding.decode_workspace_bytes(w.B, w.h, w.n_q, w.n_k, w.d)
                 if w.kind == "decode" else 0)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    # the bf16 forward goes through attn_fwd_host: host buffers in and out, the
+    # copies pipelined with the kernels over batch slices inside the call
+    host_api = w.kind == "fwd" and not f32
+    if host_api:
+        band = w.mask == inputs.MASK_BAND
+        stage = torch.empty(binding.host_buffer_bytes(w.B, w.h, w.n_q, w.n_k, w.d),
+                            dtype=torch.uint8, device=dev)
 
     def step():
+        if host_api:
+            rc = binding.attn_fwd_host_raw(
+                hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), ho.data_ptr(), hl.data_ptr(), w.B,
+                w.h, w.n_q, w.n_k, w.d, w.scale, inputs.MASK_BAND if band else w.mask,
+                None if hkl is None else hkl.data_ptr(), w.win_left if band else 0,
+                w.win_right if band else 0, stage.data_ptr(), stage.numel(), sptr)
+            if rc != 0:
+                raise binding.AttnError(rc, "attn_fwd_host")
+            return
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
@@ -549,7 +565,9 @@ def run_e2e(args, w, q, k, v, kl, dev, stream, f32):
     world = dist_env()[0]
     return {"value": world * inputs.flops(w) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms,
-            "steps": n}
+            "steps": n, "call": ("attn_fwd_host (host buffers; copies pipelined over batch "
+                                 "slices)" if host_api else
+                                 "host-to-device copies, the device call, device-to-host copies")}
 
 
 def run_e2e_bwd(args, w, q, k, v, o, lse, g, kl, dev, stream):

@@ -118,6 +118,38 @@ int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float
                      int window_right, struct CUstream_st* stream);
 
 /*
+ * attn_fwd_host -- attn_fwd (any mask_kind, as attn_fwd_strided) on HOST
+ * buffers: q, k, v are copied to the device, the forward runs there, and o
+ * (and lse, if not NULL) are copied back, all enqueued on `stream` without a
+ * host synchronisation.  The batch is cut into up to 8 slices of whole batch
+ * entries whose copies in, forward and copies out are pipelined over two
+ * internal copy streams (one each way), so the copies of one slice overlap
+ * the others' work;
+ * each (b, h) is computed by the same kernel as attn_fwd, so o and lse are
+ * bitwise those of attn_fwd.  Work enqueued on `stream` before the call
+ * completes before the first copy starts, and work enqueued after it waits
+ * for the last copy.
+ *   q, k, v, o : host bf16 [B, h, n, d_k] (contiguous); lse: host float
+ *              [B, h, n_q] or NULL; key_lens: host int32[B] for
+ *              ATTN_MASK_KEY_PADDING.  Pinned (page-locked) host memory lets
+ *              the copies run asynchronously; pageable memory is correct but
+ *              slower.  The host buffers must stay valid until the stream
+ *              reaches the end of the call's work.
+ *   dev_buf, dev_buf_bytes : caller-owned device staging of at least
+ *              attn_fwd_host_buffer_bytes(B, h, n_q, n_k, d_k) bytes,
+ *              256-byte aligned; overwritten.
+ * Other arguments and status codes as attn_fwd_strided (bf16, d_k in {16, 32,
+ * 64, 128}).
+ */
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+                  int n_q, int n_k, int d_k, float scale, int mask_kind, const int* key_lens,
+                  int window_left, int window_right, void* dev_buf, size_t dev_buf_bytes,
+                  struct CUstream_st* stream);
+
+/* Device staging bytes attn_fwd_host needs for these sizes (0 for unsupported sizes). */
+size_t attn_fwd_host_buffer_bytes(int B, int h, int n_q, int n_k, int d_k);
+
+/*
  * attn_fwd_f32 -- float32 forward on the CUDA cores (fp32 FMA, same
  * definition, same arguments with float tensors).  d_k in {16, 32, 64, 128}.
  */

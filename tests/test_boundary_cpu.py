@@ -223,3 +223,31 @@ def test_bwd_strided_arguments_rejected_on_host(lib):
     assert call(d=128) == binding.ATTN_ERR_UNSUPPORTED
     assert lib.attn_bwd_strided(A, A, A, A, A, A, A, A, A, 1, 8, 8, 8, 64, None, 0.125, 0, None,
                                 0, 0, A, 1 << 30, None) == INV   # no stride array
+
+
+def test_fwd_host_arguments_rejected_on_host(lib):
+    H = 0x20000  # a host address: only non-null is required of it
+
+    def call(q=H, o=H, B=2, d=64, mask=0, lens=None, left=0, right=0, buf=A, nbytes=1 << 30):
+        return binding.attn_fwd_host_raw(q, H, H, o, None, B, 2, 8, 8, d, 0.125, mask, lens, left,
+                                         right, buf, nbytes, None)
+    INV = binding.ATTN_ERR_INVALID_ARG
+    assert call(q=None) == INV and call(o=None) == INV
+    assert call(B=0) == INV
+    assert call(mask=5) == INV and call(mask=3, left=-1) == INV
+    assert call(mask=2, lens=None) == INV
+    assert call(buf=A + 16) == INV            # staging must be 256-byte aligned
+    assert call(buf=None) == INV
+    assert call(nbytes=1024) == INV
+    assert call(d=48) == binding.ATTN_ERR_UNSUPPORTED
+
+
+def test_fwd_host_buffer_size():
+    binding.load()
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    B, h, n_q, n_k, d = 3, 2, 100, 70, 64
+    want = (up(B * h * n_q * d * 2) * 2 + up(B * h * n_k * d * 2) * 2 + up(B * h * n_q * 4)
+            + up(B * 4))
+    assert binding.host_buffer_bytes(B, h, n_q, n_k, d) == want
+    assert binding.host_buffer_bytes(1, 1, 8, 8, 48) == 0
+    assert binding.host_buffer_bytes(0, 1, 8, 8, 64) == 0

@@ -29,7 +29,8 @@ MASK_WINDOW = 3  # attn_fwd_strided: the window of attn_fwd_window
 DECODE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 # Every entry point declared in include/attn.h.
-EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_fwd_window", "attn_fwd_strided", "attn_decode", "attn_decode_workspace_bytes",
+EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_fwd_window", "attn_fwd_strided", "attn_fwd_host",
+           "attn_fwd_host_buffer_bytes", "attn_decode", "attn_decode_workspace_bytes",
            "attn_decode_noalloc", "attn_bwd", "attn_bwd_window", "attn_bwd_strided",
            "attn_bwd_workspace_bytes",
            "attn_check", "attn_status_string",
@@ -81,6 +82,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         lib.attn_bwd.restype = i32
         lib.attn_bwd.argtypes = [vp] * 9 + [i32] * 5 + [f32, i32, vp, vp, ctypes.c_size_t, vp]
+        lib.attn_fwd_host.restype = i32
+        lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp,
+                                      i32, i32, vp, ctypes.c_size_t, vp]
+        lib.attn_fwd_host_buffer_bytes.restype = ctypes.c_size_t
+        lib.attn_fwd_host_buffer_bytes.argtypes = [i32, i32, i32, i32, i32]
         lib.attn_bwd_strided.restype = i32
         lib.attn_bwd_strided.argtypes = [vp] * 9 + [i32] * 5 + [vp, f32, i32, vp, i32, i32, vp,
                                                                  ctypes.c_size_t, vp]
@@ -257,6 +263,65 @@ def attn_fwd_strided(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: f
                               _stream_ptr(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_strided")
+    return out, lse
+
+
+def host_buffer_bytes(B: int, h: int, n_q: int, n_k: int, d: int = 64) -> int:
+    """Device staging bytes attn_fwd_host needs (0 for unsupported sizes)."""
+    return int(load().attn_fwd_host_buffer_bytes(B, h, n_q, n_k, d))
+
+
+def attn_fwd_host_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, n_k, d_k, scale, mask_kind,
+                      lens_ptr, left, right, buf_ptr, buf_bytes, stream_ptr) -> int:
+    """The C call itself (host q, k, v, o, lse, lens; device staging); returns the status."""
+    return load().attn_fwd_host(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, n_k, d_k,
+                                float(scale), int(mask_kind), lens_ptr, int(left), int(right),
+                                buf_ptr, int(buf_bytes), stream_ptr)
+
+
+def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+                  mask: int = MASK_NONE, key_lens: torch.Tensor | None = None,
+                  window: tuple[int, int] | None = None, out: torch.Tensor | None = None,
+                  lse: torch.Tensor | None = None, with_lse: bool = True,
+                  buf: torch.Tensor | None = None, device=None, stream=None):
+    """attn_fwd on host (CPU) bf16 [B, h, n, d] tensors, pinned for asynchronous copies:
+    copies in, forward and copies out pipelined over batch slices on the device.
+    Returns host (o, lse); they are complete once ``stream`` has reached the call's
+    end (``check()`` synchronises)."""
+    for t in (q, k, v):
+        if t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 host [B, h, n, d] tensors")
+    B, h, n_q, d = q.shape
+    n_k = k.shape[2]
+    if tuple(k.shape) != (B, h, n_k, d) or tuple(v.shape) != (B, h, n_k, d):
+        raise ValueError("k and v must be [B, h, n_k, d] with q's B, h, d")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    kl, left, right = None, 0, 0
+    if window is not None:
+        mask, (left, right) = MASK_WINDOW, window
+    if mask == MASK_KEY_PADDING:
+        if key_lens is None:
+            raise ValueError("key padding needs key_lens")
+        kl = key_lens
+        if kl.dtype != torch.int32 or kl.is_cuda or kl.numel() != B or not kl.is_contiguous():
+            raise ValueError("key_lens must be a contiguous int32 host tensor of B entries")
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty((B, h, n_q, d), dtype=q.dtype, pin_memory=pin)
+    if out.is_cuda or tuple(out.shape) != (B, h, n_q, d) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous host [B, h, n_q, d] tensor")
+    if lse is None and with_lse:
+        lse = torch.empty((B, h, n_q), dtype=torch.float32, pin_memory=pin)
+    need = host_buffer_bytes(B, h, n_q, n_k, d)
+    if buf is None or buf.numel() * buf.element_size() < need:
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        buf = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    rc = attn_fwd_host_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, h, n_q, n_k, d,
+                           scale, int(mask), _ptr(kl), left, right, _ptr(buf),
+                           buf.numel() * buf.element_size(), _stream_ptr(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_host")
     return out, lse
 
 

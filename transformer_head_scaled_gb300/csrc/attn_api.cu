@@ -22,11 +22,25 @@ __device__ int g_status;
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultLimitNs = 2000000000ull;
 
+// attn_fwd_host splits the batch into at most this many slices, so that the
+// copies of one slice overlap the kernel and the copies of its neighbours.
+constexpr int kHostSlices = 8;
+// Copy streams per direction (slices alternate between them); two measured no
+// faster than one: the host link, not the copy engines, sets the rate.
+constexpr int kCopyStreams = 1;
+
 struct DeviceInfo {
   bool ready = false;
   bool supported = false;
   int num_sms = 0;
   int* status = nullptr;
+  // attn_fwd_host: copy-in and copy-out streams and the events that order
+  // them with the caller's stream (created on first use; issued under
+  // host_mu so that concurrent callers do not share an event in flight).
+  cudaStream_t copy_in[kCopyStreams] = {}, copy_out[kCopyStreams] = {};
+  cudaEvent_t ev_start = nullptr, ev_done[kCopyStreams] = {};
+  cudaEvent_t ev_in[kHostSlices] = {}, ev_kernel[kHostSlices] = {};
+  std::mutex host_mu;
 };
 
 std::mutex g_mu;
@@ -246,6 +260,60 @@ int encode_decode_maps(CUtensorMap* maps, const void* k_cache, const void* v_cac
   return encode_3d(&maps[3], v_cache, d_k, L_max, bh, 32);
 }
 
+// Device staging of attn_fwd_host: Q, K, V, O (bf16), LSE (fp32) and the key
+// lengths (int32), each at a 256-byte boundary, for the whole batch.
+struct HostLayout {
+  size_t q, k, v, o, lse, lens, bytes;
+};
+
+HostLayout host_layout(int B, int h, int n_q, int n_k, int d) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t bh = static_cast<size_t>(B) * h;
+  HostLayout l;
+  size_t off = 0;
+  l.q = off;
+  off += up(bh * n_q * d * 2);
+  l.k = off;
+  off += up(bh * n_k * d * 2);
+  l.v = off;
+  off += up(bh * n_k * d * 2);
+  l.o = off;
+  off += up(bh * n_q * d * 2);
+  l.lse = off;
+  off += up(bh * n_q * 4);
+  l.lens = off;
+  off += up(static_cast<size_t>(B) * 4);
+  l.bytes = off;
+  return l;
+}
+
+// The copy streams and events of attn_fwd_host, created once per device.
+int host_streams(DeviceInfo* di) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (di->copy_in[0] != nullptr) return ATTN_OK;
+  cudaError_t e;
+  cudaStream_t st[2 * kCopyStreams];
+  for (int i = 0; i < 2 * kCopyStreams; ++i)
+    if ((e = cudaStreamCreateWithFlags(&st[i], cudaStreamNonBlocking)) != cudaSuccess)
+      return cuda_fail(e);
+  cudaEvent_t* evs[1 + kCopyStreams + 2 * kHostSlices];
+  int n = 0;
+  evs[n++] = &di->ev_start;
+  for (int i = 0; i < kCopyStreams; ++i) evs[n++] = &di->ev_done[i];
+  for (int i = 0; i < kHostSlices; ++i) {
+    evs[n++] = &di->ev_in[i];
+    evs[n++] = &di->ev_kernel[i];
+  }
+  for (int i = 0; i < n; ++i)
+    if ((e = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming)) != cudaSuccess)
+      return cuda_fail(e);
+  for (int i = kCopyStreams - 1; i >= 0; --i) {
+    di->copy_out[i] = st[kCopyStreams + i];
+    di->copy_in[i] = st[i];  // copy_in[0] last: marks the set as complete
+  }
+  return ATTN_OK;
+}
+
 LaunchCtx make_ctx(const DeviceInfo& di, cudaStream_t stream) {
   LaunchCtx ctx;
   ctx.num_sms = di.num_sms;
@@ -347,6 +415,111 @@ int attn_fwd_strided(const void* q, const void* k, const void* v, void* o, float
   cudaError_t e = launch_fwd_tc(pb, tmq, tmk, tmv, tmo, make_ctx(*di, stream));
   if (e != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(1);
+  return ATTN_OK;
+}
+
+size_t attn_fwd_host_buffer_bytes(int B, int h, int n_q, int n_k, int d_k) {
+  if (B < 1 || h < 1 || n_q < 1 || n_k < 1 || !tc_head_size(d_k)) return 0;
+  if (static_cast<long long>(B) * h > 0x7fffffffLL) return 0;
+  return host_layout(B, h, n_q, n_k, d_k).bytes;
+}
+
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int h,
+                  int n_q, int n_k, int d_k, float scale, int mask_kind, const int* key_lens,
+                  int window_left, int window_right, void* dev_buf, size_t dev_buf_bytes,
+                  struct CUstream_st* stream) {
+  const bool window = mask_kind == ATTN_MASK_WINDOW;
+  if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_WINDOW) return ATTN_ERR_INVALID_ARG;
+  if (window && (window_left < 0 || window_right < 0)) return ATTN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (mask_kind == ATTN_MASK_KEY_PADDING && key_lens == nullptr) return ATTN_ERR_INVALID_ARG;
+  // sizes, scale and the device-side limits, checked as for attn_fwd on the
+  // staging buffer (the host buffers need no alignment)
+  const void* stage = dev_buf;
+  int rc = check_common(stage, stage, stage, stage, nullptr, B, h, n_q, n_k, d_k, scale,
+                        mask_kind == ATTN_MASK_KEY_PADDING ? ATTN_MASK_KEY_PADDING : ATTN_MASK_NONE,
+                        static_cast<const int*>(stage), 2);
+  if (rc != ATTN_OK) return rc;
+  if (reinterpret_cast<uintptr_t>(dev_buf) & 255u) return ATTN_ERR_INVALID_ARG;
+  if (!tc_head_size(d_k)) return ATTN_ERR_UNSUPPORTED;
+  const HostLayout lay = host_layout(B, h, n_q, n_k, d_k);
+  if (dev_buf_bytes < lay.bytes) return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(&di)) != ATTN_OK) return rc;
+  if ((rc = host_streams(di)) != ATTN_OK) return rc;
+  std::lock_guard<std::mutex> lock(di->host_mu);
+
+  uint8_t* dbuf = static_cast<uint8_t*>(dev_buf);
+  const size_t qrow = static_cast<size_t>(h) * n_q * d_k * 2;  // bytes of one batch entry
+  const size_t krow = static_cast<size_t>(h) * n_k * d_k * 2;
+  const size_t lrow = static_cast<size_t>(h) * n_q * 4;
+  const bool padding = mask_kind == ATTN_MASK_KEY_PADDING;
+  const int reach = n_q + n_k;
+  const int slices = B < kHostSlices ? B : kHostSlices;
+  cudaError_t e;
+  // the staging buffer and the host buffers may still be in use by work
+  // enqueued earlier on the caller's stream
+  if ((e = cudaEventRecord(di->ev_start, stream)) != cudaSuccess) return cuda_fail(e);
+  for (int i = 0; i < kCopyStreams; ++i) {
+    if ((e = cudaStreamWaitEvent(di->copy_in[i], di->ev_start, 0)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(di->copy_out[i], di->ev_start, 0)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  for (int s = 0; s < slices; ++s) {
+    const int b0 = static_cast<int>(static_cast<long long>(B) * s / slices);
+    const int b1 = static_cast<int>(static_cast<long long>(B) * (s + 1) / slices);
+    const int nb = b1 - b0;
+    uint8_t* dq = dbuf + lay.q + b0 * qrow;
+    uint8_t* dk = dbuf + lay.k + b0 * krow;
+    uint8_t* dv = dbuf + lay.v + b0 * krow;
+    uint8_t* dout = dbuf + lay.o + b0 * qrow;
+    float* dlse = reinterpret_cast<float*>(dbuf + lay.lse + b0 * lrow);
+    int* dlens = reinterpret_cast<int*>(dbuf + lay.lens) + b0;
+    cudaStream_t cin = di->copy_in[s % kCopyStreams], cout = di->copy_out[s % kCopyStreams];
+    // copy in (one copy per tensor slice)
+    if ((e = cudaMemcpyAsync(dq, static_cast<const uint8_t*>(q) + b0 * qrow, nb * qrow, h2d,
+                             cin)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaMemcpyAsync(dk, static_cast<const uint8_t*>(k) + b0 * krow, nb * krow, h2d,
+                             cin)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaMemcpyAsync(dv, static_cast<const uint8_t*>(v) + b0 * krow, nb * krow, h2d,
+                             cin)) != cudaSuccess)
+      return cuda_fail(e);
+    if (padding && (e = cudaMemcpyAsync(dlens, key_lens + b0, nb * sizeof(int), h2d, cin)) !=
+                       cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaEventRecord(di->ev_in[s], cin)) != cudaSuccess) return cuda_fail(e);
+    // the forward of this slice on the caller's stream
+    if ((e = cudaStreamWaitEvent(stream, di->ev_in[s], 0)) != cudaSuccess) return cuda_fail(e);
+    CUtensorMap tmq, tmk, tmv, tmo;
+    if ((rc = encode_fwd_maps(&tmq, &tmk, &tmv, &tmo, dq, dk, dv, dout, d_k, n_q, n_k, h, nb,
+                              nullptr)) != ATTN_OK)
+      return rc;
+    Problem pb{dq, dk, dv, dout, lse ? dlse : nullptr, nb, h, n_q, n_k, d_k, scale,
+               window ? static_cast<int>(kMaskBand) : mask_kind, padding ? dlens : nullptr,
+               window_left < reach ? window_left : reach,
+               window_right < reach ? window_right : reach};
+    if ((e = launch_fwd_tc(pb, tmq, tmk, tmv, tmo, make_ctx(*di, stream))) != cudaSuccess)
+      return cuda_fail(e);
+    g_launches.fetch_add(1);
+    if ((e = cudaEventRecord(di->ev_kernel[s], stream)) != cudaSuccess) return cuda_fail(e);
+    // copy out
+    if ((e = cudaStreamWaitEvent(cout, di->ev_kernel[s], 0)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemcpyAsync(static_cast<uint8_t*>(o) + b0 * qrow, dout, nb * qrow, d2h, cout)) !=
+        cudaSuccess)
+      return cuda_fail(e);
+    if (lse && (e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + b0 * lrow, dlse, nb * lrow,
+                                    d2h, cout)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  // the caller's stream resumes once every copy out is done
+  for (int i = 0; i < kCopyStreams; ++i) {
+    if ((e = cudaEventRecord(di->ev_done[i], di->copy_out[i])) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(stream, di->ev_done[i], 0)) != cudaSuccess) return cuda_fail(e);
+  }
   return ATTN_OK;
 }
 
