@@ -167,7 +167,8 @@ int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float
  *   k_cache, v_cache : bf16 [B, h, L_max, d_k]; rows past cache_lens[b] are
  *              never used.
  *   o, lse   : bf16 [B, h, n_q, d_k] and float [B, h, n_q] (lse may be NULL).
- *   d_k      : 64 (else ATTN_ERR_UNSUPPORTED); B*h <= 65535.
+ *   d_k      : 16, 32, 64 or 128 (else ATTN_ERR_UNSUPPORTED; 64 runs the TMA-fed
+ *              kernel, the others a kernel with plain loads); B*h <= 65535.
  *   cache_lens : device int32[B] (clamped to [0, L_max] on the device), or
  *              NULL when every sequence fills the cache.
  *   workspace, workspace_bytes : caller-owned device scratch of at least

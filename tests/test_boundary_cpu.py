@@ -99,9 +99,10 @@ def test_decode_arguments_rejected_on_host(lib):
     assert call(scale=float("nan")) == INV
     assert call(lens=A + 2) == INV
     assert call(n_q=9) == UNS
-    assert call(d=32) == UNS
+    assert call(d=48) == UNS and call(d=256) == UNS   # head sizes 16, 32, 64, 128 only
     assert call(B=1 << 9, h=1 << 8) == UNS      # B*h beyond the grid's y extent
     assert lib.attn_decode_workspace_bytes(1, 1, 9, 8, 64) == 0   # unsupported sizes
+    assert lib.attn_decode_workspace_bytes(1, 1, 1, 8, 48) == 0
 
 
 def test_diag_entry_points_validate(lib):

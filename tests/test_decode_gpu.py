@@ -39,8 +39,8 @@ def _check(o, lse, q, k, v, lens, scale):
         assert np.abs(lse[fin] - l_ref[fin]).max() <= 1e-3
 
 
-def _case(B, h, n_q, L_max, lens, seed=0):
-    w = Workload("dec", B, h, n_q, L_max, 64, MASK_KEY_PADDING, "bf16", kind="decode")
+def _case(B, h, n_q, L_max, lens, seed=0, d=64):
+    w = Workload("dec", B, h, n_q, L_max, d, MASK_KEY_PADDING, "bf16", kind="decode")
     q, k, v, _ = inputs.make_inputs(w, device="cuda", seeds=(seed, seed + 1, seed + 2, seed + 3))
     kl = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
     return w, q, k, v, kl
@@ -134,5 +134,42 @@ def test_decode_many_units_every_row(B, h, L_max):
     lens[:3] = [0, L_max, 1]
     w, q, k, v, kl = _case(B, h, 1, L_max, lens.tolist(), seed=3)
     o, lse = binding.attn_decode(q, k, v, kl, scale=w.scale)
+    binding.check()
+    _check(o, lse, q, k, v, kl, w.scale)
+
+
+
+@pytest.mark.parametrize("d", [16, 32, 128])
+@pytest.mark.parametrize("n_q", [1, 3, 8])
+@pytest.mark.parametrize("shape", [(3, 2, 300), (1, 2, 4096), (40, 4, 200)])
+def test_decode_other_head_sizes_match_oracle(d, n_q, shape):
+    """Head sizes 16, 32 and 128 (Table 3 of the paper): split and unsplit caches,
+    lengths from empty to full, every output row checked."""
+    B, h, L = shape
+    rng = np.random.default_rng(B + 7 * n_q + d)
+    lens = rng.integers(0, L + 1, size=B)
+    lens[0] = L
+    if B > 2:
+        lens[1] = 0
+    w, q, k, v, kl = _case(B, h, n_q, L, lens.tolist(), seed=5, d=d)
+    o, lse = binding.attn_decode(q, k, v, kl, scale=w.scale)
+    binding.check()
+    _check(o, lse, q, k, v, kl, w.scale)
+
+
+@pytest.mark.parametrize("d", [16, 128])
+def test_decode_other_head_sizes_without_lengths_and_nan_tail(d):
+    """No lengths: the whole cache; with lengths, NaN past them is never read."""
+    w, q, k, v, _ = _case(2, 3, 2, 700, None, seed=6, d=d)
+    o, lse = binding.attn_decode(q, k, v, None, scale=w.scale)
+    binding.check()
+    _check(o, lse, q, k, v, None, w.scale)
+    lens = [5, 300]
+    w, q, k, v, kl = _case(2, 2, 1, 512, lens, seed=7, d=d)
+    k2, v2 = k.clone(), v.clone()
+    for b, L in enumerate(lens):
+        k2[b, :, L:] = float("nan")
+        v2[b, :, L:] = float("nan")
+    o, lse = binding.attn_decode(q, k2, v2, kl, scale=w.scale)
     binding.check()
     _check(o, lse, q, k, v, kl, w.scale)

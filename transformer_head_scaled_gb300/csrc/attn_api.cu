@@ -541,10 +541,11 @@ int attn_fwd_f32(const float* q, const float* k, const float* v, float* o, float
 }
 
 size_t attn_decode_workspace_bytes(int B, int h, int n_q, int L_max, int d_k) {
-  if (B < 1 || h < 1 || n_q < 1 || n_q > kDecodeMaxQueries || L_max < 1 || d_k != 64) return 0;
+  if (B < 1 || h < 1 || n_q < 1 || n_q > kDecodeMaxQueries || L_max < 1 || !tc_head_size(d_k))
+    return 0;
   DeviceInfo* di = nullptr;
   if (device_info(&di) != ATTN_OK) return 0;
-  return decode_plan(B, h, n_q, L_max, di->num_sms).workspace_bytes;
+  return decode_plan(B, h, n_q, L_max, d_k, di->num_sms).workspace_bytes;
 }
 
 int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
@@ -554,17 +555,18 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o
                         ATTN_MASK_NONE, nullptr, 2);
   if (rc != ATTN_OK) return rc;
   if (cache_lens && (reinterpret_cast<uintptr_t>(cache_lens) & 3u)) return ATTN_ERR_INVALID_ARG;
-  if (d_k != 64 || n_q > kDecodeMaxQueries) return ATTN_ERR_UNSUPPORTED;
+  if (!tc_head_size(d_k) || n_q > kDecodeMaxQueries) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * h > 65535) return ATTN_ERR_UNSUPPORTED;  // grid.y
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di)) != ATTN_OK) return rc;
-  const DecodePlan plan = decode_plan(B, h, n_q, L_max, di->num_sms);
+  const DecodePlan plan = decode_plan(B, h, n_q, L_max, d_k, di->num_sms);
   if (plan.workspace_bytes > 0 &&
       (workspace == nullptr || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)))
     return ATTN_ERR_INVALID_ARG;
   CUtensorMap maps[4];
-  if ((rc = encode_decode_maps(maps, k_cache, v_cache, d_k, L_max, B, h)) != ATTN_OK) return rc;
-  DecodeProblem pb{q, k_cache, v_cache, o, lse, B, h, n_q, L_max, scale, cache_lens};
+  if (d_k == 64 && (rc = encode_decode_maps(maps, k_cache, v_cache, d_k, L_max, B, h)) != ATTN_OK)
+    return rc;
+  DecodeProblem pb{q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, scale, cache_lens};
   cudaError_t e = launch_decode(pb, maps, plan, static_cast<float*>(workspace),
                                 make_ctx(*di, stream));
   if (e != cudaSuccess) return cuda_fail(e);
@@ -579,17 +581,18 @@ int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                         ATTN_MASK_NONE, nullptr, 2);
   if (rc != ATTN_OK) return rc;
   if (cache_lens && (reinterpret_cast<uintptr_t>(cache_lens) & 3u)) return ATTN_ERR_INVALID_ARG;
-  if (d_k != 64 || n_q > kDecodeMaxQueries) return ATTN_ERR_UNSUPPORTED;
+  if (!tc_head_size(d_k) || n_q > kDecodeMaxQueries) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * h > 65535) return ATTN_ERR_UNSUPPORTED;  // grid.y
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di)) != ATTN_OK) return rc;
-  const DecodePlan plan = decode_plan(B, h, n_q, L_max, di->num_sms);
+  const DecodePlan plan = decode_plan(B, h, n_q, L_max, d_k, di->num_sms);
   if (plan.workspace_bytes > ATTN_DECODE_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_SCRATCH_TOO_SMALL;
   void* scratch = nullptr;
   if ((rc = scratch_on_device(&scratch)) != ATTN_OK) return rc;
   CUtensorMap maps[4];
-  if ((rc = encode_decode_maps(maps, k_cache, v_cache, d_k, L_max, B, h)) != ATTN_OK) return rc;
-  DecodeProblem pb{q, k_cache, v_cache, o, lse, B, h, n_q, L_max, scale, cache_lens};
+  if (d_k == 64 && (rc = encode_decode_maps(maps, k_cache, v_cache, d_k, L_max, B, h)) != ATTN_OK)
+    return rc;
+  DecodeProblem pb{q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, scale, cache_lens};
   cudaError_t e = launch_decode(pb, maps, plan, static_cast<float*>(scratch),
                                 make_ctx(*di, stream));
   if (e != cudaSuccess) return cuda_fail(e);

@@ -430,7 +430,172 @@ __global__ void __launch_bounds__(THREADS, 3)
   }
 }
 
+// The same decoding step for the head sizes 16, 32 and 128, on the CUDA cores
+// with plain 16-byte loads of the cache rows (no TMA ring): one CTA of four
+// warps per work unit, each warp taking every fourth group of 32 keys of the
+// unit's chunk with its own online softmax (float32 P), the warps merged in
+// shared memory at the end as above.  For the scores lane l takes key l of
+// the group; for P V, LPK lanes share one key row, each holding DPL
+// consecutive output columns, and KPI = 32 / LPK keys are taken at once.
+template <int D, int NQ>
+__global__ void __launch_bounds__(THREADS)
+    attn_decode_rows_kernel(const __nv_bfloat16* __restrict__ kc,
+                            const __nv_bfloat16* __restrict__ vc, const DecParams p) {
+  constexpr int LPK = D < 32 ? D : 32;  // lanes per key row in P V
+  constexpr int KPI = 32 / LPK;         // keys per P V step
+  constexpr int DPL = D / LPK;          // output columns per lane
+  __shared__ float sq[NQ][D];           // queries, pre-scaled by scale*log2(e)
+  __shared__ float red[NWARPS][NQ][D + 2];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x;
+  const int bh = u / p.splits;
+  int L = p.L_max;
+  if (p.cache_lens != nullptr) L = min(max(__ldg(p.cache_lens + bh / p.H), 0), p.L_max);
+  const int begin = (u % p.splits) * p.chunk;
+  const int end = min(L, begin + p.chunk);
+  for (int e = threadIdx.x; e < NQ * D; e += THREADS)
+    sq[e / D][e % D] =
+        __bfloat162float(p.q[(static_cast<size_t>(bh) * NQ + e / D) * D + e % D]) * p.scale_log2;
+  __syncthreads();
+
+  const size_t head = static_cast<size_t>(bh) * p.L_max;  // first cache row of this head
+  const int kofs = lane / LPK;        // this lane's key inside a P V step
+  const int c0 = (lane % LPK) * DPL;  // and its first output column
+  float m[NQ], l[NQ], o[NQ][DPL];
+#pragma unroll
+  for (int qi = 0; qi < NQ; ++qi) {
+    m[qi] = -INFINITY;
+    l[qi] = 0.f;
+#pragma unroll
+    for (int t = 0; t < DPL; ++t) o[qi][t] = 0.f;
+  }
+  for (int g0 = begin + warp * 32; g0 < end; g0 += NWARPS * 32) {
+    // ---- scores of key g0 + lane for every query
+    const int j = g0 + lane;
+    const bool valid = j < end;
+    float s[NQ];
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) s[qi] = 0.f;
+    if (valid) {
+      const uint4* krow = reinterpret_cast<const uint4*>(kc + (head + j) * D);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 w = __ldg(krow + c);
+        const float kf[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                             bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s[qi] = fmaf(sq[qi][c * 8 + e], kf[e], s[qi]);
+      }
+    }
+    // ---- online softmax over the group
+    float pr[NQ];
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) {
+      const float sv = valid ? s[qi] : -INFINITY;
+      const float mn = fmaxf(m[qi], warp_max(sv));
+      const float base = mn == -INFINITY ? 0.f : mn;
+      const float alpha = ex2(m[qi] - base);  // 0 when m = -inf
+      l[qi] *= alpha;
+#pragma unroll
+      for (int t = 0; t < DPL; ++t) o[qi][t] *= alpha;
+      m[qi] = mn;
+      pr[qi] = ex2(sv - base);  // 0 for keys past the chunk
+      l[qi] += pr[qi];
+    }
+    // ---- P V: rows past the valid keys are never read
+    const int nvalid = min(32, end - g0);
+    for (int jj = 0; jj < nvalid; jj += KPI) {
+      const int key = jj + kofs;
+      const bool kv = key < nvalid;
+      float vf[DPL];
+      if (kv) {
+        const __nv_bfloat16* vrow = vc + (head + g0 + key) * D + c0;
+        if constexpr (DPL == 4) {
+          const uint2 w = __ldg(reinterpret_cast<const uint2*>(vrow));
+          vf[0] = bf16lo(w.x), vf[1] = bf16hi(w.x), vf[2] = bf16lo(w.y), vf[3] = bf16hi(w.y);
+        } else {
+#pragma unroll
+          for (int t = 0; t < DPL; ++t) vf[t] = __bfloat162float(vrow[t]);
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) vf[t] = 0.f;
+      }
+#pragma unroll
+      for (int qi = 0; qi < NQ; ++qi) {
+        const float pj = __shfl_sync(0xffffffffu, pr[qi], key & 31);
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) o[qi][t] = fmaf(kv ? pj : 0.f, vf[t], o[qi][t]);
+      }
+    }
+  }
+  // lanes that took other keys of the same P V steps hold the same columns
+#pragma unroll
+  for (int qi = 0; qi < NQ; ++qi)
+#pragma unroll
+    for (int t = 0; t < DPL; ++t)
+#pragma unroll
+      for (int x = LPK; x < 32; x <<= 1) o[qi][t] += __shfl_xor_sync(0xffffffffu, o[qi][t], x);
+  // ---- merge the four warps' states in shared memory
+#pragma unroll
+  for (int qi = 0; qi < NQ; ++qi) {
+    const float lw = warp_sum(l[qi]);
+    if (kofs == 0) {
+#pragma unroll
+      for (int t = 0; t < DPL; ++t) red[warp][qi][c0 + t] = o[qi][t];
+    }
+    if (lane == 0) {
+      red[warp][qi][D] = m[qi];
+      red[warp][qi][D + 1] = lw;
+    }
+  }
+  __syncthreads();
+  for (int qi = warp; qi < NQ; qi += NWARPS) {
+    float mm = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) mm = fmaxf(mm, red[w][qi][D]);
+    const float base = mm == -INFINITY ? 0.f : mm;
+    float f[NWARPS], ll = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) {
+      f[w] = ex2(red[w][qi][D] - base);
+      ll += f[w] * red[w][qi][D + 1];
+    }
+    const size_t row = static_cast<size_t>(bh) * NQ + qi;
+    float* dst = p.splits == 1
+                     ? nullptr
+                     : p.part + ((static_cast<size_t>(bh) * p.splits + (u % p.splits)) * NQ + qi) *
+                                    (D + 2);
+    const float inv = ll > 0.f ? 1.f / ll : 0.f;
+    for (int t2 = lane; t2 < D / 2; t2 += 32) {  // column pairs
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < NWARPS; ++w) {
+        a0 += f[w] * red[w][qi][2 * t2];
+        a1 += f[w] * red[w][qi][2 * t2 + 1];
+      }
+      if (dst == nullptr) {
+        reinterpret_cast<uint32_t*>(p.o + row * D)[t2] = pack_bf16x2(a0 * inv, a1 * inv);
+      } else {
+        dst[2 * t2] = a0;
+        dst[2 * t2 + 1] = a1;
+      }
+    }
+    if (lane == 0) {
+      if (dst == nullptr) {
+        if (p.lse != nullptr) p.lse[row] = ll > 0.f ? (mm + __log2f(ll)) * LN2 : -INFINITY;
+      } else {
+        dst[D] = mm;
+        dst[D + 1] = ll;
+      }
+    }
+  }
+}
+
 // One warp per (b, h, query): merge the chunks' partial results.
+template <int D>
 __global__ void __launch_bounds__(128)
     attn_decode_combine_kernel(const float* __restrict__ part, __nv_bfloat16* __restrict__ o,
                                float* __restrict__ lse, int rows, int n_q, int splits) {
@@ -440,19 +605,25 @@ __global__ void __launch_bounds__(128)
   const int bh = row / n_q, qi = row % n_q;
   float mm = -INFINITY;
   for (int sp = 0; sp < splits; ++sp)
-    mm = fmaxf(mm, part[((static_cast<size_t>(bh) * splits + sp) * n_q + qi) * (DK + 2) + DK]);
+    mm = fmaxf(mm, part[((static_cast<size_t>(bh) * splits + sp) * n_q + qi) * (D + 2) + D]);
   const float base = mm == -INFINITY ? 0.f : mm;
-  float ll = 0.f, a0 = 0.f, a1 = 0.f;
+  float ll = 0.f;
   for (int sp = 0; sp < splits; ++sp) {
-    const float* src = part + ((static_cast<size_t>(bh) * splits + sp) * n_q + qi) * (DK + 2);
-    const float f = ex2(src[DK] - base);
-    ll += f * src[DK + 1];
-    a0 += f * src[2 * lane];
-    a1 += f * src[2 * lane + 1];
+    const float* src = part + ((static_cast<size_t>(bh) * splits + sp) * n_q + qi) * (D + 2);
+    ll += ex2(src[D] - base) * src[D + 1];
   }
   const float inv = ll > 0.f ? 1.f / ll : 0.f;
-  reinterpret_cast<uint32_t*>(o + static_cast<size_t>(row) * DK)[lane] =
-      pack_bf16x2(a0 * inv, a1 * inv);
+  for (int t2 = lane; t2 < D / 2; t2 += 32) {  // column pairs
+    float a0 = 0.f, a1 = 0.f;
+    for (int sp = 0; sp < splits; ++sp) {
+      const float* src = part + ((static_cast<size_t>(bh) * splits + sp) * n_q + qi) * (D + 2);
+      const float f = ex2(src[D] - base);
+      a0 += f * src[2 * t2];
+      a1 += f * src[2 * t2 + 1];
+    }
+    reinterpret_cast<uint32_t*>(o + static_cast<size_t>(row) * D)[t2] =
+        pack_bf16x2(a0 * inv, a1 * inv);
+  }
   if (lane == 0 && lse != nullptr) lse[row] = ll > 0.f ? (mm + __log2f(ll)) * LN2 : -INFINITY;
 }
 
@@ -473,7 +644,32 @@ cudaError_t launch_split(const CUtensorMap* maps, const DecParams& p, int BH, in
 
 }  // namespace
 
-DecodePlan decode_plan(int B, int H, int n_q, int L_max, int num_sms) {
+template <int D, int NQ>
+cudaError_t launch_rows(const DecodeProblem& pb, const DecParams& p, int units,
+                        cudaStream_t stream) {
+  attn_decode_rows_kernel<D, NQ><<<units, THREADS, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(pb.k_cache), static_cast<const __nv_bfloat16*>(pb.v_cache),
+      p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_rows_d(const DecodeProblem& pb, const DecParams& p, int units,
+                          cudaStream_t stream) {
+  switch (pb.n_q) {
+    case 1: return launch_rows<D, 1>(pb, p, units, stream);
+    case 2: return launch_rows<D, 2>(pb, p, units, stream);
+    case 3: return launch_rows<D, 3>(pb, p, units, stream);
+    case 4: return launch_rows<D, 4>(pb, p, units, stream);
+    case 5: return launch_rows<D, 5>(pb, p, units, stream);
+    case 6: return launch_rows<D, 6>(pb, p, units, stream);
+    case 7: return launch_rows<D, 7>(pb, p, units, stream);
+    case 8: return launch_rows<D, 8>(pb, p, units, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+DecodePlan decode_plan(int B, int H, int n_q, int L_max, int d, int num_sms) {
   DecodePlan plan;
   const long long bh = static_cast<long long>(B) * H;
   const int max_tiles = (L_max + KT - 1) / KT;
@@ -487,7 +683,7 @@ DecodePlan decode_plan(int B, int H, int n_q, int L_max, int num_sms) {
   plan.splits = splits;
   plan.chunk = tiles_per * KT;
   plan.workspace_bytes =
-      splits > 1 ? static_cast<size_t>(bh) * splits * n_q * (DK + 2) * sizeof(float) : 0;
+      splits > 1 ? static_cast<size_t>(bh) * splits * n_q * (d + 2) * sizeof(float) : 0;
   return plan;
 }
 
@@ -510,7 +706,15 @@ cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap* maps, cons
   p.status = ctx.status;
   const int BH = pb.B * pb.H;
   cudaError_t err;
-  switch (pb.n_q) {
+  if (pb.d != DK) {
+    const int units = BH * plan.splits;
+    switch (pb.d) {
+      case 16: err = launch_rows_d<16>(pb, p, units, ctx.stream); break;
+      case 32: err = launch_rows_d<32>(pb, p, units, ctx.stream); break;
+      case 128: err = launch_rows_d<128>(pb, p, units, ctx.stream); break;
+      default: return cudaErrorInvalidValue;
+    }
+  } else switch (pb.n_q) {
     case 1: err = launch_split<1>(maps, p, BH, ctx.num_sms, ctx.stream); break;
     case 2: err = launch_split<2>(maps, p, BH, ctx.num_sms, ctx.stream); break;
     case 3: err = launch_split<3>(maps, p, BH, ctx.num_sms, ctx.stream); break;
@@ -523,8 +727,17 @@ cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap* maps, cons
   }
   if (err != cudaSuccess || plan.splits == 1) return err;
   const int rows = BH * pb.n_q;
-  attn_decode_combine_kernel<<<(rows + 3) / 4, 128, 0, ctx.stream>>>(
-      workspace, p.o, p.lse, rows, pb.n_q, plan.splits);
+  const unsigned blocks = static_cast<unsigned>((rows + 3) / 4);
+  switch (pb.d) {
+    case 16: attn_decode_combine_kernel<16><<<blocks, 128, 0, ctx.stream>>>(
+                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits); break;
+    case 32: attn_decode_combine_kernel<32><<<blocks, 128, 0, ctx.stream>>>(
+                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits); break;
+    case 64: attn_decode_combine_kernel<64><<<blocks, 128, 0, ctx.stream>>>(
+                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits); break;
+    default: attn_decode_combine_kernel<128><<<blocks, 128, 0, ctx.stream>>>(
+                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits); break;
+  }
   return cudaGetLastError();
 }
 

@@ -50,12 +50,12 @@ cudaError_t launch_fwd_f32(const Problem& pb, const LaunchCtx& ctx);
 constexpr int kDecodeMaxQueries = 8;
 
 struct DecodeProblem {
-  const void* q;        // bf16 [B, H, n_q, 64]
-  const void* k_cache;  // bf16 [B, H, L_max, 64]
+  const void* q;        // bf16 [B, H, n_q, d]
+  const void* k_cache;  // bf16 [B, H, L_max, d]
   const void* v_cache;
-  void* o;              // bf16 [B, H, n_q, 64]
+  void* o;              // bf16 [B, H, n_q, d]
   float* lse;           // [B, H, n_q] or null
-  int B, H, n_q, L_max;
+  int B, H, n_q, L_max, d;  // d in {16, 32, 64, 128}
   float scale;
   const int* cache_lens;  // device int32[B] or null (all L_max valid)
 };
@@ -67,9 +67,10 @@ struct DecodePlan {
   int chunk;  // keys per split, a multiple of the 128-key tile
   size_t workspace_bytes;
 };
-DecodePlan decode_plan(int B, int H, int n_q, int L_max, int num_sms);
-// maps[0..3]: K cache, V cache as 3-D (64, L_max, B*H) bf16 with a
-// (64, 128, 1) box, then the same with a (64, 32, 1) box for partial last
+DecodePlan decode_plan(int B, int H, int n_q, int L_max, int d, int num_sms);
+// maps[0..3] (d = 64; unused for the other head sizes, whose kernel reads the
+// cache with plain loads): K cache, V cache as 3-D (64, L_max, B*H) bf16 with
+// a (64, 128, 1) box, then the same with a (64, 32, 1) box for partial last
 // tiles; all with 128-byte swizzle.  workspace holds plan.workspace_bytes.
 cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap* maps, const DecodePlan& plan,
                           float* workspace, const LaunchCtx& ctx);

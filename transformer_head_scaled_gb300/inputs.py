@@ -88,6 +88,14 @@ WORKLOADS = {
     "decode_long": Workload("decode_long", 32, 16, 1, 4096, 64, MASK_KEY_PADDING, "bf16",
                             lens_lo=2048, kind="decode",
                             note="big model, 8 sentences x beam 4, cache up to 4096"),
+    # The decoding step of the base model split into other head counts
+    # ("Attention Is All You Need", Table 3, rows (A)): the same cache bytes.
+    "decode_beam_h4_d128": Workload("decode_beam_h4_d128", 256, 4, 1, 512, 128, MASK_KEY_PADDING,
+                                    "bf16", kind="decode",
+                                    note="decode_beam with 4 heads of 128"),
+    "decode_beam_h16_d32": Workload("decode_beam_h16_d32", 256, 16, 1, 512, 32, MASK_KEY_PADDING,
+                                    "bf16", kind="decode",
+                                    note="decode_beam with 16 heads of 32"),
     # Other splits of the base model's d_model = 512 into heads ("Attention
     # Is All You Need", Table 3, rows (A)): h x d_k = 4 x 128, 16 x 32, 32 x 16.
     "base_h4_d128": Workload("base_h4_d128", 64, 4, 512, 512, 128, MASK_NONE, "bf16",
