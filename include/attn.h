@@ -183,6 +183,21 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o
  * (0 when no split is needed, or for unsupported sizes). */
 size_t attn_decode_workspace_bytes(int B, int h, int n_q, int L_max, int d_k);
 
+/*
+ * attn_decode_strided -- attn_decode on a query, a cache and an output of any
+ * batch, head and row strides, e.g. a cache laid out [B, L_max, h, d] as many
+ * decoders keep it.  Element (b, hh, i, t) of each tensor X is
+ * x[b*s[0] + hh*s[1] + i*s[2] + t]; strides is a host array of 12 element
+ * counts, three (b, h, row) per tensor in the order q, k_cache, v_cache, o,
+ * each > 0 and a multiple of 8 (16 bytes); d is contiguous; lse stays
+ * contiguous [B, h, n_q].  Other arguments, the workspace size and the status
+ * codes as attn_decode.
+ */
+int attn_decode_strided(const void* q, const void* k_cache, const void* v_cache, void* o,
+                        float* lse, int B, int h, int n_q, int L_max, int d_k,
+                        const int64_t* strides, float scale, const int* cache_lens,
+                        void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
 /* Size of the fixed scratch array behind attn_decode_noalloc (1 MiB). */
 #define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (1u << 20)
 

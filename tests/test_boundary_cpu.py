@@ -252,3 +252,22 @@ def test_fwd_host_buffer_size():
     assert binding.host_buffer_bytes(B, h, n_q, n_k, d) == want
     assert binding.host_buffer_bytes(1, 1, 8, 8, 48) == 0
     assert binding.host_buffer_bytes(0, 1, 8, 8, 64) == 0
+
+
+def test_decode_strided_arguments_rejected_on_host(lib):
+    good = [(8 * 64 * 4, 64, 4 * 64)] * 4
+
+    def call(strides=good, d=64, q=A):
+        return binding.attn_decode_strided_raw(q, A, A, A, None, 1, 4, 1, 8, d, strides, 0.125,
+                                               None, None, 0, None)
+    INV = binding.ATTN_ERR_INVALID_ARG
+    for i in range(4):
+        bad = list(good)
+        bad[i] = (8 * 64 * 4, 64 + 4, 4 * 64)
+        assert call(strides=bad) == INV, i
+        bad[i] = (8 * 64 * 4, 64, -256)
+        assert call(strides=bad) == INV, i
+    assert call(q=None) == INV
+    assert call(d=48) == binding.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_decode_strided(A, A, A, A, None, 1, 4, 1, 8, 64, None, 0.125, None, None, 0,
+                                   None) == INV

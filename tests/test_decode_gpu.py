@@ -173,3 +173,23 @@ def test_decode_other_head_sizes_without_lengths_and_nan_tail(d):
     o, lse = binding.attn_decode(q, k2, v2, kl, scale=w.scale)
     binding.check()
     _check(o, lse, q, k, v, kl, w.scale)
+
+
+@pytest.mark.parametrize("d", [64, 128, 16])
+@pytest.mark.parametrize("B,h,n_q,L_max", [(6, 4, 2, 700), (1, 2, 1, 4096)])
+def test_decode_strided_caches_equal_contiguous(d, B, h, n_q, L_max):
+    """Caches kept [B, L_max, h, d] and outputs written into a [B, n_q, h, d]
+    buffer: the same results as the contiguous call, bit for bit, and the oracle's."""
+    rng = np.random.default_rng(d + B)
+    lens = rng.integers(0, L_max + 1, size=B)
+    lens[0] = L_max
+    w, q, k, v, kl = _case(B, h, n_q, L_max, lens.tolist(), seed=8, d=d)
+    ks, vs = (t.transpose(1, 2).contiguous().transpose(1, 2) for t in (k, v))  # [B, L, h, d]
+    qs = q.transpose(1, 2).contiguous().transpose(1, 2)
+    out = torch.full((B, n_q, h, d), float("nan"), dtype=torch.bfloat16,
+                     device="cuda").transpose(1, 2)
+    o, lse = binding.attn_decode_strided(qs, ks, vs, kl, scale=w.scale, out=out)
+    o_ref, lse_ref = binding.attn_decode(q, k, v, kl, scale=w.scale)
+    binding.check()
+    assert torch.equal(o.contiguous(), o_ref) and torch.equal(lse, lse_ref)
+    _check(o.contiguous(), lse, q, k, v, kl, w.scale)

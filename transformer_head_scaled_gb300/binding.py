@@ -30,7 +30,8 @@ DECODE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 # Every entry point declared in include/attn.h.
 EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_fwd_window", "attn_fwd_strided", "attn_fwd_host",
-           "attn_fwd_host_buffer_bytes", "attn_decode", "attn_decode_workspace_bytes",
+           "attn_fwd_host_buffer_bytes", "attn_decode", "attn_decode_strided",
+           "attn_decode_workspace_bytes",
            "attn_decode_noalloc", "attn_bwd", "attn_bwd_window", "attn_bwd_strided",
            "attn_bwd_workspace_bytes",
            "attn_check", "attn_status_string",
@@ -82,6 +83,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         lib.attn_bwd.restype = i32
         lib.attn_bwd.argtypes = [vp] * 9 + [i32] * 5 + [f32, i32, vp, vp, ctypes.c_size_t, vp]
+        lib.attn_decode_strided.restype = i32
+        lib.attn_decode_strided.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, f32,
+                                            vp, vp, ctypes.c_size_t, vp]
         lib.attn_fwd_host.restype = i32
         lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp,
                                       i32, i32, vp, ctypes.c_size_t, vp]
@@ -342,6 +346,55 @@ def attn_decode_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, L_max, d, sc
     """The C call itself, on raw device pointers; returns the status code."""
     return load().attn_decode(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, L_max, d,
                               float(scale), lens_ptr, ws_ptr, int(ws_bytes), stream_ptr)
+
+
+def attn_decode_strided_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, L_max, d, strides,
+                            scale, lens_ptr, ws_ptr, ws_bytes, stream_ptr) -> int:
+    """The C call itself; ``strides`` = four (b, h, n) element-stride triples for q, k_cache,
+    v_cache, o."""
+    flat = (ctypes.c_int64 * 12)(*[int(x) for st in strides for x in st])
+    return load().attn_decode_strided(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, L_max, d,
+                                      ctypes.cast(flat, ctypes.c_void_p), float(scale), lens_ptr,
+                                      ws_ptr, int(ws_bytes), stream_ptr)
+
+
+def attn_decode_strided(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                        cache_lens: torch.Tensor | None = None, scale: float | None = None,
+                        out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, stream=None):
+    """attn_decode on [B, h, n, d] bf16 views with any strides over the first three
+    dimensions and a contiguous last one (e.g. a [B, L_max, h, d] cache seen as
+    ``cache.transpose(1, 2)``); ``out`` may be a strided view too."""
+    for t in (q, k_cache, v_cache):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or t.stride(-1) != 1:
+            raise ValueError("q, k_cache, v_cache must be bf16 CUDA [B, h, n, d] views with unit "
+                             "last stride")
+    B, h, n_q, d = q.shape
+    L_max = k_cache.shape[2]
+    if tuple(k_cache.shape) != (B, h, L_max, d) or tuple(v_cache.shape) != (B, h, L_max, d):
+        raise ValueError("caches must be [B, h, L_max, d] with q's B, h, d")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if cache_lens is not None and (cache_lens.dtype != torch.int32 or not cache_lens.is_cuda
+                                   or cache_lens.numel() != B or not cache_lens.is_contiguous()):
+        raise ValueError("cache_lens must be a contiguous int32 CUDA tensor of B entries")
+    if out is None:
+        out = torch.empty((B, h, n_q, d), dtype=q.dtype, device=q.device)
+    if tuple(out.shape) != (B, h, n_q, d) or out.stride(-1) != 1:
+        raise ValueError("out must be a [B, h, n_q, d] view with unit last stride")
+    if lse is None:
+        lse = torch.empty((B, h, n_q), dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes(B, h, n_q, L_max, d)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    strides = [t.stride()[:3] for t in (q, k_cache, v_cache, out)]
+    rc = attn_decode_strided_raw(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), B,
+                                 h, n_q, L_max, d, strides, scale, _ptr(cache_lens),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream_ptr(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_strided")
+    return out, lse
 
 
 def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

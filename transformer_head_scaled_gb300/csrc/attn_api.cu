@@ -120,26 +120,6 @@ int check_common(const void* q, const void* k, const void* v, const void* o, con
   return ATTN_OK;
 }
 
-// (d, n, B*H) bf16 view with a (min(d, 64), rows, 1) box in the widest
-// swizzle its 2*min(d, 64)-byte rows fit: 128, 64 or 32 bytes (d = 128 is
-// copied as two 64-column boxes).
-int encode_3d(CUtensorMap* map, const void* base, int d, int n, long long bh, int box_rows) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n),
-                        static_cast<cuuint64_t>(bh)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                           static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(n)};
-  const int inner = d < 64 ? d : 64;
-  const CUtensorMapSwizzle swz = inner == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
-                                 : inner == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                               : CU_TENSOR_MAP_SWIZZLE_32B;
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(inner), static_cast<cuuint32_t>(box_rows), 1u};
-  cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? ATTN_OK : cuda_fail(cudaErrorInvalidValue);
-}
-
 // (d, n, B*H) fp32 view with a (min(d, 32), 64, 1) box in the swizzle of its
 // 4*min(d, 32)-byte rows (the backward's dQ accumulator, added into by TMA
 // reduce).
@@ -251,13 +231,12 @@ int scratch_on_device(void** out) {
 
 // K and V caches with 128-key boxes, then with 32-key boxes for partial tiles.
 int encode_decode_maps(CUtensorMap* maps, const void* k_cache, const void* v_cache, int d_k,
-                       int L_max, int B, int h) {
-  const long long bh = static_cast<long long>(B) * h;
+                       int L_max, int B, int h, Strides sk, Strides sv) {
   int rc;
-  if ((rc = encode_3d(&maps[0], k_cache, d_k, L_max, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&maps[1], v_cache, d_k, L_max, bh, 128)) != ATTN_OK) return rc;
-  if ((rc = encode_3d(&maps[2], k_cache, d_k, L_max, bh, 32)) != ATTN_OK) return rc;
-  return encode_3d(&maps[3], v_cache, d_k, L_max, bh, 32);
+  if ((rc = encode_4d(&maps[0], k_cache, d_k, L_max, h, B, sk, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_4d(&maps[1], v_cache, d_k, L_max, h, B, sv, 128)) != ATTN_OK) return rc;
+  if ((rc = encode_4d(&maps[2], k_cache, d_k, L_max, h, B, sk, 32)) != ATTN_OK) return rc;
+  return encode_4d(&maps[3], v_cache, d_k, L_max, h, B, sv, 32);
 }
 
 // Device staging of attn_fwd_host: Q, K, V, O (bf16), LSE (fp32) and the key
@@ -548,9 +527,17 @@ size_t attn_decode_workspace_bytes(int B, int h, int n_q, int L_max, int d_k) {
   return decode_plan(B, h, n_q, L_max, d_k, di->num_sms).workspace_bytes;
 }
 
-int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
-                int B, int h, int n_q, int L_max, int d_k, float scale, const int* cache_lens,
-                void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
+}  // extern "C"
+
+namespace attn {
+namespace {
+// st: strides of q, k_cache, v_cache, o, or null for contiguous tensors.
+// scratch_noalloc: take the partials' space from the library's own array
+// instead of the caller's workspace.
+static int decode_impl(const void* q, const void* k_cache, const void* v_cache, void* o,
+                       float* lse, int B, int h, int n_q, int L_max, int d_k, const Strides* st,
+                       float scale, const int* cache_lens, void* workspace,
+                       size_t workspace_bytes, bool scratch_noalloc, struct CUstream_st* stream) {
   int rc = check_common(q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, scale,
                         ATTN_MASK_NONE, nullptr, 2);
   if (rc != ATTN_OK) return rc;
@@ -560,44 +547,61 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di)) != ATTN_OK) return rc;
   const DecodePlan plan = decode_plan(B, h, n_q, L_max, d_k, di->num_sms);
-  if (plan.workspace_bytes > 0 &&
-      (workspace == nullptr || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)))
+  if (scratch_noalloc) {
+    if (plan.workspace_bytes > ATTN_DECODE_NOALLOC_SCRATCH_BYTES)
+      return ATTN_ERR_SCRATCH_TOO_SMALL;
+    if ((rc = scratch_on_device(&workspace)) != ATTN_OK) return rc;
+  } else if (plan.workspace_bytes > 0 && (workspace == nullptr ||
+                                          workspace_bytes < plan.workspace_bytes ||
+                                          !aligned16(workspace))) {
     return ATTN_ERR_INVALID_ARG;
+  }
+  const Strides sq = st ? st[0] : bhsd(h, n_q, d_k), sk = st ? st[1] : bhsd(h, L_max, d_k),
+                sv = st ? st[2] : bhsd(h, L_max, d_k), so = st ? st[3] : bhsd(h, n_q, d_k);
   CUtensorMap maps[4];
-  if (d_k == 64 && (rc = encode_decode_maps(maps, k_cache, v_cache, d_k, L_max, B, h)) != ATTN_OK)
+  if (d_k == 64 &&
+      (rc = encode_decode_maps(maps, k_cache, v_cache, d_k, L_max, B, h, sk, sv)) != ATTN_OK)
     return rc;
-  DecodeProblem pb{q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, scale, cache_lens};
+  DecodeProblem pb{q,  k_cache, v_cache, o,          lse, B,  h,  n_q, L_max,
+                   d_k, scale,  cache_lens, sq, sk, sv, so};
   cudaError_t e = launch_decode(pb, maps, plan, static_cast<float*>(workspace),
                                 make_ctx(*di, stream));
   if (e != cudaSuccess) return cuda_fail(e);
   g_launches.fetch_add(plan.splits > 1 ? 2 : 1);
   return ATTN_OK;
 }
+}  // namespace
+}  // namespace attn
+
+extern "C" {
+
+int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                int B, int h, int n_q, int L_max, int d_k, float scale, const int* cache_lens,
+                void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
+  return decode_impl(q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, nullptr, scale,
+                     cache_lens, workspace, workspace_bytes, false, stream);
+}
 
 int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o,
                         float* lse, int B, int h, int n_q, int L_max, int d_k, float scale,
                         const int* cache_lens, struct CUstream_st* stream) {
-  int rc = check_common(q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, scale,
-                        ATTN_MASK_NONE, nullptr, 2);
-  if (rc != ATTN_OK) return rc;
-  if (cache_lens && (reinterpret_cast<uintptr_t>(cache_lens) & 3u)) return ATTN_ERR_INVALID_ARG;
-  if (!tc_head_size(d_k) || n_q > kDecodeMaxQueries) return ATTN_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * h > 65535) return ATTN_ERR_UNSUPPORTED;  // grid.y
-  DeviceInfo* di = nullptr;
-  if ((rc = device_info(&di)) != ATTN_OK) return rc;
-  const DecodePlan plan = decode_plan(B, h, n_q, L_max, d_k, di->num_sms);
-  if (plan.workspace_bytes > ATTN_DECODE_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_SCRATCH_TOO_SMALL;
-  void* scratch = nullptr;
-  if ((rc = scratch_on_device(&scratch)) != ATTN_OK) return rc;
-  CUtensorMap maps[4];
-  if (d_k == 64 && (rc = encode_decode_maps(maps, k_cache, v_cache, d_k, L_max, B, h)) != ATTN_OK)
-    return rc;
-  DecodeProblem pb{q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, scale, cache_lens};
-  cudaError_t e = launch_decode(pb, maps, plan, static_cast<float*>(scratch),
-                                make_ctx(*di, stream));
-  if (e != cudaSuccess) return cuda_fail(e);
-  g_launches.fetch_add(plan.splits > 1 ? 2 : 1);
-  return ATTN_OK;
+  return decode_impl(q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, nullptr, scale,
+                     cache_lens, nullptr, 0, true, stream);
+}
+
+int attn_decode_strided(const void* q, const void* k_cache, const void* v_cache, void* o,
+                        float* lse, int B, int h, int n_q, int L_max, int d_k,
+                        const int64_t* strides, float scale, const int* cache_lens,
+                        void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
+  if (strides == nullptr) return ATTN_ERR_INVALID_ARG;
+  Strides st[4];
+  for (int i = 0; i < 4; ++i) {
+    st[i] = Strides{strides[3 * i], strides[3 * i + 1], strides[3 * i + 2]};
+    if (!stride_ok(st[i].b) || !stride_ok(st[i].h) || !stride_ok(st[i].n))
+      return ATTN_ERR_INVALID_ARG;
+  }
+  return decode_impl(q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, st, scale, cache_lens,
+                     workspace, workspace_bytes, false, stream);
 }
 
 size_t attn_bwd_workspace_bytes(int B, int h, int n_q, int d_k) {

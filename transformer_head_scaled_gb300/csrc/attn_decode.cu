@@ -67,6 +67,7 @@ struct DecParams {
   const __nv_bfloat16* q;
   const int* cache_lens;  // may be null: every key of the cache is valid
   __nv_bfloat16* o;
+  RowStrides sq, sk, sv, so;  // element strides of q, k, v, o (batch entry, head, row)
   float* lse;
   float* part;  // workspace: [B*h][splits][n_q][DK + 2] (m, l, O), or null
   int H, BH, n_q, L_max, splits, chunk;
@@ -74,6 +75,11 @@ struct DecParams {
   uint64_t limit_ns;
   int* status;
 };
+
+// Element offset of row i of head bh (= b * H + h) in a strided tensor.
+__device__ __forceinline__ long long row_off(const RowStrides& s, int bh, int H, int i) {
+  return (bh / H) * s.b + (bh % H) * s.h + static_cast<long long>(i) * s.n;
+}
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -228,16 +234,18 @@ __global__ void __launch_bounds__(THREADS, 3)
     const uint32_t bar = smem_u32(&sm.full[slot]);
     if (rem >= KT) {
       mbar_arrive_expect_tx(bar, 2 * TILE_BYTES);
-      tma_load_3d(smem_u32(sm.k[slot]), &tmk, bar, 0, key0, pbh);
-      tma_load_3d(smem_u32(sm.v[slot]), &tmv, bar, 0, key0, pbh);
+      tma_load_4d(smem_u32(sm.k[slot]), &tmk, bar, 0, key0, pbh % p.H, pbh / p.H);
+      tma_load_4d(smem_u32(sm.v[slot]), &tmv, bar, 0, key0, pbh % p.H, pbh / p.H);
     } else {
       // a partial last tile: only the 32-key boxes that hold valid keys (the
       // rows after them keep stale data, which the consumers never use)
       const int nbox = (rem + TAIL - 1) / TAIL;
       mbar_arrive_expect_tx(bar, 2 * nbox * TAIL_BYTES);
       for (int i = 0; i < nbox; ++i) {
-        tma_load_3d(smem_u32(sm.k[slot]) + i * TAIL_BYTES, &tmk_tail, bar, 0, key0 + i * TAIL, pbh);
-        tma_load_3d(smem_u32(sm.v[slot]) + i * TAIL_BYTES, &tmv_tail, bar, 0, key0 + i * TAIL, pbh);
+        tma_load_4d(smem_u32(sm.k[slot]) + i * TAIL_BYTES, &tmk_tail, bar, 0, key0 + i * TAIL,
+                    pbh % p.H, pbh / p.H);
+        tma_load_4d(smem_u32(sm.v[slot]) + i * TAIL_BYTES, &tmv_tail, bar, 0, key0 + i * TAIL,
+                    pbh % p.H, pbh / p.H);
       }
     }
     ++pt;
@@ -258,7 +266,7 @@ __global__ void __launch_bounds__(THREADS, 3)
     for (int i = 0; i < QPT; ++i) {
       const int e = threadIdx.x + i * THREADS;
       qv[i] = (u < units && e < NQ * DK)
-                  ? __bfloat162float(p.q[(static_cast<size_t>(bh) * NQ + e / DK) * DK + e % DK])
+                  ? __bfloat162float(p.q[row_off(p.sq, bh, p.H, e / DK) + e % DK])
                   : 0.f;
     }
   };
@@ -400,7 +408,8 @@ __global__ void __launch_bounds__(THREADS, 3)
       const size_t row = static_cast<size_t>(bh) * NQ + qi;
       if (p.splits == 1) {
         const float inv = ll > 0.f ? 1.f / ll : 0.f;
-        reinterpret_cast<uint32_t*>(p.o + row * DK)[lane] = pack_bf16x2(a0 * inv, a1 * inv);
+        reinterpret_cast<uint32_t*>(p.o + row_off(p.so, bh, p.H, qi))[lane] =
+            pack_bf16x2(a0 * inv, a1 * inv);
         if (lane == 0 && p.lse != nullptr)
           p.lse[row] = ll > 0.f ? (mm + __log2f(ll)) * LN2 : -INFINITY;
       } else {
@@ -455,10 +464,11 @@ __global__ void __launch_bounds__(THREADS)
   const int end = min(L, begin + p.chunk);
   for (int e = threadIdx.x; e < NQ * D; e += THREADS)
     sq[e / D][e % D] =
-        __bfloat162float(p.q[(static_cast<size_t>(bh) * NQ + e / D) * D + e % D]) * p.scale_log2;
+        __bfloat162float(p.q[row_off(p.sq, bh, p.H, e / D) + e % D]) * p.scale_log2;
   __syncthreads();
 
-  const size_t head = static_cast<size_t>(bh) * p.L_max;  // first cache row of this head
+  const __nv_bfloat16* khead = kc + row_off(p.sk, bh, p.H, 0);  // this head's cache rows
+  const __nv_bfloat16* vhead = vc + row_off(p.sv, bh, p.H, 0);
   const int kofs = lane / LPK;        // this lane's key inside a P V step
   const int c0 = (lane % LPK) * DPL;  // and its first output column
   float m[NQ], l[NQ], o[NQ][DPL];
@@ -477,7 +487,7 @@ __global__ void __launch_bounds__(THREADS)
 #pragma unroll
     for (int qi = 0; qi < NQ; ++qi) s[qi] = 0.f;
     if (valid) {
-      const uint4* krow = reinterpret_cast<const uint4*>(kc + (head + j) * D);
+      const uint4* krow = reinterpret_cast<const uint4*>(khead + j * p.sk.n);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
         const uint4 w = __ldg(krow + c);
@@ -506,12 +516,13 @@ __global__ void __launch_bounds__(THREADS)
     }
     // ---- P V: rows past the valid keys are never read
     const int nvalid = min(32, end - g0);
-    for (int jj = 0; jj < nvalid; jj += KPI) {
+    const long long vstep = KPI * p.sv.n;
+    const __nv_bfloat16* vrow = vhead + (g0 + kofs) * p.sv.n + c0;  // advanced by vstep
+    for (int jj = 0; jj < nvalid; jj += KPI, vrow += vstep) {
       const int key = jj + kofs;
       const bool kv = key < nvalid;
       float vf[DPL];
       if (kv) {
-        const __nv_bfloat16* vrow = vc + (head + g0 + key) * D + c0;
         if constexpr (DPL == 4) {
           const uint2 w = __ldg(reinterpret_cast<const uint2*>(vrow));
           vf[0] = bf16lo(w.x), vf[1] = bf16hi(w.x), vf[2] = bf16lo(w.y), vf[3] = bf16hi(w.y);
@@ -577,7 +588,8 @@ __global__ void __launch_bounds__(THREADS)
         a1 += f[w] * red[w][qi][2 * t2 + 1];
       }
       if (dst == nullptr) {
-        reinterpret_cast<uint32_t*>(p.o + row * D)[t2] = pack_bf16x2(a0 * inv, a1 * inv);
+        reinterpret_cast<uint32_t*>(p.o + row_off(p.so, bh, p.H, qi))[t2] =
+            pack_bf16x2(a0 * inv, a1 * inv);
       } else {
         dst[2 * t2] = a0;
         dst[2 * t2 + 1] = a1;
@@ -598,7 +610,8 @@ __global__ void __launch_bounds__(THREADS)
 template <int D>
 __global__ void __launch_bounds__(128)
     attn_decode_combine_kernel(const float* __restrict__ part, __nv_bfloat16* __restrict__ o,
-                               float* __restrict__ lse, int rows, int n_q, int splits) {
+                               float* __restrict__ lse, int rows, int n_q, int splits, int H,
+                               RowStrides so) {
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);  // (bh * n_q + qi)
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -621,8 +634,7 @@ __global__ void __launch_bounds__(128)
       a0 += f * src[2 * t2];
       a1 += f * src[2 * t2 + 1];
     }
-    reinterpret_cast<uint32_t*>(o + static_cast<size_t>(row) * D)[t2] =
-        pack_bf16x2(a0 * inv, a1 * inv);
+    reinterpret_cast<uint32_t*>(o + row_off(so, bh, H, qi))[t2] = pack_bf16x2(a0 * inv, a1 * inv);
   }
   if (lane == 0 && lse != nullptr) lse[row] = ll > 0.f ? (mm + __log2f(ll)) * LN2 : -INFINITY;
 }
@@ -701,6 +713,10 @@ cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap* maps, cons
   p.L_max = pb.L_max;
   p.splits = plan.splits;
   p.chunk = plan.chunk;
+  p.sq = pb.sq;
+  p.sk = pb.sk;
+  p.sv = pb.sv;
+  p.so = pb.so;
   p.scale_log2 = pb.scale * 1.4426950408889634f;
   p.limit_ns = ctx.limit_ns;
   p.status = ctx.status;
@@ -730,13 +746,13 @@ cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap* maps, cons
   const unsigned blocks = static_cast<unsigned>((rows + 3) / 4);
   switch (pb.d) {
     case 16: attn_decode_combine_kernel<16><<<blocks, 128, 0, ctx.stream>>>(
-                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits); break;
+                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits, pb.H, pb.so); break;
     case 32: attn_decode_combine_kernel<32><<<blocks, 128, 0, ctx.stream>>>(
-                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits); break;
+                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits, pb.H, pb.so); break;
     case 64: attn_decode_combine_kernel<64><<<blocks, 128, 0, ctx.stream>>>(
-                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits); break;
+                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits, pb.H, pb.so); break;
     default: attn_decode_combine_kernel<128><<<blocks, 128, 0, ctx.stream>>>(
-                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits); break;
+                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits, pb.H, pb.so); break;
   }
   return cudaGetLastError();
 }

@@ -46,6 +46,12 @@ int fwd_tc_kv_rows(int d);
 // fp32 SIMT path (d in {16, 32, 64, 128}).
 cudaError_t launch_fwd_f32(const Problem& pb, const LaunchCtx& ctx);
 
+// Element strides of a [B, H, n, d] view across batch entries, heads and rows
+// (d contiguous).
+struct RowStrides {
+  long long b, h, n;
+};
+
 // Decode path (n_q <= kDecodeMaxQueries new queries against a cache).
 constexpr int kDecodeMaxQueries = 8;
 
@@ -58,6 +64,7 @@ struct DecodeProblem {
   int B, H, n_q, L_max, d;  // d in {16, 32, 64, 128}
   float scale;
   const int* cache_lens;  // device int32[B] or null (all L_max valid)
+  RowStrides sq, sk, sv, so;  // element strides (batch entry, head, row) of q, k, v, o
 };
 
 // How the cache of each head is split across CTAs; workspace_bytes = 0 when
@@ -69,17 +76,11 @@ struct DecodePlan {
 };
 DecodePlan decode_plan(int B, int H, int n_q, int L_max, int d, int num_sms);
 // maps[0..3] (d = 64; unused for the other head sizes, whose kernel reads the
-// cache with plain loads): K cache, V cache as 3-D (64, L_max, B*H) bf16 with
-// a (64, 128, 1) box, then the same with a (64, 32, 1) box for partial last
-// tiles; all with 128-byte swizzle.  workspace holds plan.workspace_bytes.
+// cache with plain loads): K cache, V cache as 4-D (64, L_max, H, B) bf16 with
+// a (64, 128, 1, 1) box, then the same with a (64, 32, 1, 1) box for partial
+// last tiles; all with 128-byte swizzle.  workspace holds plan.workspace_bytes.
 cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap* maps, const DecodePlan& plan,
                           float* workspace, const LaunchCtx& ctx);
-
-// Element strides of a [B, H, n, d] view across batch entries, heads and rows
-// (d contiguous).
-struct RowStrides {
-  long long b, h, n;
-};
 
 // Backward (d = 16, 32 or 64; bf16): gradients of the forward above.
 struct BwdProblem {
