@@ -456,21 +456,22 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
     uint8_t* dout = dbuf + lay.o + b0 * qrow;
     float* dlse = reinterpret_cast<float*>(dbuf + lay.lse + b0 * lrow);
     int* dlens = reinterpret_cast<int*>(dbuf + lay.lens) + b0;
-    cudaStream_t cin = di->copy_in[s % kCopyStreams], cout = di->copy_out[s % kCopyStreams];
+    cudaStream_t copy_in = di->copy_in[s % kCopyStreams];
+    cudaStream_t copy_out = di->copy_out[s % kCopyStreams];
     // copy in (one copy per tensor slice)
     if ((e = cudaMemcpyAsync(dq, static_cast<const uint8_t*>(q) + b0 * qrow, nb * qrow, h2d,
-                             cin)) != cudaSuccess)
+                             copy_in)) != cudaSuccess)
       return cuda_fail(e);
     if ((e = cudaMemcpyAsync(dk, static_cast<const uint8_t*>(k) + b0 * krow, nb * krow, h2d,
-                             cin)) != cudaSuccess)
+                             copy_in)) != cudaSuccess)
       return cuda_fail(e);
     if ((e = cudaMemcpyAsync(dv, static_cast<const uint8_t*>(v) + b0 * krow, nb * krow, h2d,
-                             cin)) != cudaSuccess)
+                             copy_in)) != cudaSuccess)
       return cuda_fail(e);
-    if (padding && (e = cudaMemcpyAsync(dlens, key_lens + b0, nb * sizeof(int), h2d, cin)) !=
+    if (padding && (e = cudaMemcpyAsync(dlens, key_lens + b0, nb * sizeof(int), h2d, copy_in)) !=
                        cudaSuccess)
       return cuda_fail(e);
-    if ((e = cudaEventRecord(di->ev_in[s], cin)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaEventRecord(di->ev_in[s], copy_in)) != cudaSuccess) return cuda_fail(e);
     // the forward of this slice on the caller's stream
     if ((e = cudaStreamWaitEvent(stream, di->ev_in[s], 0)) != cudaSuccess) return cuda_fail(e);
     CUtensorMap tmq, tmk, tmv, tmo;
@@ -486,12 +487,12 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
     g_launches.fetch_add(1);
     if ((e = cudaEventRecord(di->ev_kernel[s], stream)) != cudaSuccess) return cuda_fail(e);
     // copy out
-    if ((e = cudaStreamWaitEvent(cout, di->ev_kernel[s], 0)) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaMemcpyAsync(static_cast<uint8_t*>(o) + b0 * qrow, dout, nb * qrow, d2h, cout)) !=
-        cudaSuccess)
+    if ((e = cudaStreamWaitEvent(copy_out, di->ev_kernel[s], 0)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemcpyAsync(static_cast<uint8_t*>(o) + b0 * qrow, dout, nb * qrow, d2h,
+                             copy_out)) != cudaSuccess)
       return cuda_fail(e);
     if (lse && (e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + b0 * lrow, dlse, nb * lrow,
-                                    d2h, cout)) != cudaSuccess)
+                                    d2h, copy_out)) != cudaSuccess)
       return cuda_fail(e);
   }
   // the caller's stream resumes once every copy out is done
