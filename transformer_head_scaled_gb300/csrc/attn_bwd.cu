@@ -46,9 +46,12 @@
 //               item needs it); Q and its constant tile (3 stages) and dO (2
 //               stages) per query tile;
 //   warp  13    tensor-memory owner and MMA issuer.
-// Tensor memory (512 columns): S'^T [0,128)  dP'^T [128,256)  dV [256,320)
-// dK [320,384)  dQ [384,448)  P^T [448,512) (bf16 pairs).  Keys are the 128
-// lanes of all but dQ, whose lanes are queries.
+// Tensor memory (512 columns, w = max(d, 32) for head size d in {16, 32,
+// 64}): S'^T [0,128)  dP'^T [128,256)  dV, dK, dQ w columns each from 256,
+// then P^T (64 columns of bf16 pairs); at d = 64 dV [256,320) dK [320,384)
+// dQ [384,448) P^T [448,512).  Keys are the 128 lanes of all but dQ, whose
+// lanes are queries.  Q, K, V, dO tiles are [128 x d] in the swizzle of their
+// 2d-byte rows; dS^T is [128 x 128] at every d.
 // Products per tile pair t (all 128-row M; * = from tensor memory):
 //   S'^T = K Q^T (+1 b^T)    dP'^T = V dO^T (+1 (-D)^T)    dV += P^T* dO
 //   dK += dS^T Q             dQ = dS K
