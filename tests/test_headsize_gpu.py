@@ -82,14 +82,23 @@ def test_head_size_window_matches_oracle(d):
 
 
 @pytest.mark.parametrize("name", ["base_h4_d128", "base_h16_d32", "base_h32_d16"])
-def test_head_size_full_workload_sampled_rows(name):
+def test_head_size_full_workload_whole_tensor(name):
+    """The benchmark's head-size workloads, every element against the oracle."""
     w = inputs.WORKLOADS[name]
     q, k, v, kl = inputs.make_inputs(w, device="cuda")
     o, lse = binding.attn_fwd(q, k, v, scale=w.scale, mask=w.mask, key_lens=kl)
     binding.check()
-    total = w.B * w.h * w.n_q
-    rng = np.random.default_rng(17)
-    rows = np.unique(np.concatenate([np.arange(0, total, 127), rng.integers(0, total, size=512)]))
-    o_ref, l_ref = oracle.attn_rows(q, k, v, rows, w.scale, w.mask, kl)
-    idx = torch.as_tensor(rows, device="cuda")
-    _compare(o.reshape(-1, w.d)[idx], lse.reshape(-1)[idx], o_ref, l_ref)
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, w.scale, w.mask, kl)
+    _compare(o, lse, o_ref, l_ref)
+
+
+@pytest.mark.parametrize("d", [16, 32, 128])
+def test_head_size_many_items_per_cta(d):
+    """B=16, h=8, n=1024 under the causal mask: 512 work items, several per
+    persistent CTA, each element compared."""
+    q, k, v = _inputs(16, 8, 1024, 1024, d, seed=31)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = binding.attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale=scale, mask=MASK_CAUSAL)
+    binding.check()
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, scale, MASK_CAUSAL)
+    _compare(o, lse, o_ref, l_ref)

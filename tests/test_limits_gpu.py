@@ -109,17 +109,22 @@ def test_backward_long_keys_uniform_softmax():
     assert rel_k <= 5e-3, rel_k
 
 
-def test_many_heads_sampled_against_oracle():
+def test_many_heads_against_oracle():
     """131072 (b, h) pairs of short sequences: the item index space, head and
-    batch coordinates at their largest in the benchmark's range and beyond."""
+    batch coordinates at their largest in the benchmark's range and beyond;
+    every element compared, the oracle run over slices of 1024 batch entries."""
     B, h, n, d = 8192, 16, 40, 64
     w = inputs.Workload("heads", B, h, n, n, d, MASK_NONE, "bf16")
     q, k, v, _ = inputs.make_inputs(w, device="cuda")
     o, lse = binding.attn_fwd(q, k, v)
     binding.check()
-    for bb, hh in [(0, 0), (B - 1, h - 1), (5000, 7), (B // 2, 0)]:
-        sub = [t[bb: bb + 1, hh: hh + 1].cpu() for t in (q, k, v)]
+    err_sum, err_max, count = 0.0, 0.0, 0
+    for b0 in range(0, B, 1024):
+        sub = [t[b0: b0 + 1024] for t in (q, k, v)]
         o_ref, l_ref = oracle.attn_fwd(*sub, 0.125, MASK_NONE, None)
-        err = np.abs(o[bb, hh].float().cpu().numpy() - o_ref[0, 0])
-        assert err.max() <= 2e-2 and err.mean() <= 2e-3
-        assert np.abs(lse[bb, hh].cpu().numpy() - l_ref[0, 0]).max() <= 1e-3
+        err = np.abs(o[b0: b0 + 1024].float().cpu().numpy() - o_ref)
+        err_sum += float(err.sum())
+        err_max = max(err_max, float(err.max()))
+        count += err.size
+        assert np.abs(lse[b0: b0 + 1024].cpu().numpy() - l_ref).max() <= 1e-3
+    assert err_max <= 2e-2 and err_sum / count <= 2e-3
