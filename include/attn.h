@@ -217,9 +217,10 @@ int attn_decode_strided(const void* q, const void* k_cache, const void* v_cache,
  * partials would not fit return ATTN_ERR_SCRATCH_TOO_SMALL (use attn_decode
  * with a workspace of attn_decode_workspace_bytes(...) instead).
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  All calls share the one array and it keeps whatever the last call
+ * The first call on a device whose sizes split the cache (the calls for
+ * which attn_decode_workspace_bytes is not 0; only those use the array)
+ * looks up the array's device address, once per device, with that device
+ * current; make such a call before any stream capture.  All calls share the one array and it keeps whatever the last call
  * left in it; nothing in it needs to start at zero (every partial is written
  * before it is read).  Calls whose kernels may overlap on the GPU (different
  * streams, or host threads on the same device) race on the array: order them

@@ -8,20 +8,24 @@ library keeps a fixed scratch array of its own (1 MiB per device, held until
 the process exits) and attn_decode_noalloc uses it in place of the workspace
 that attn_decode takes from the caller.
 
-These tests call it through the C ABI and check that it returns what
-attn_decode returns with a caller-allocated workspace, within the tolerances
-the other parity tests use, on two calls in a row (the second call finds the
-first call's leftovers in the shared array), and that sizes whose partial
-results do not fit the array are refused.  The file is collected last, so a
-failure here never hides the outcome of another test; it also runs on its own
-in a fresh process.
+These tests call it through the C ABI and check it against the float64
+oracle (the decoding step is the forward with a key-padding mask over the
+cache) and against attn_decode with a caller-allocated workspace, within the
+tolerances the other parity tests use, on calls in a row that share the
+array: a split cache, a second problem whose partials need more of the array
+than the first one's, an empty cache entry, and the plain-load kernel of the
+other head sizes.  Sizes whose partials do not fit the array are refused.
+The file is collected last, so a failure here never hides the outcome of
+another test; it also runs on its own in a fresh process.
 """
 import ctypes
+import math
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from transformer_head_scaled_gb300 import binding, inputs
 from transformer_head_scaled_gb300.inputs import MASK_KEY_PADDING, Workload
 
@@ -34,12 +38,15 @@ def lib():
         pytest.fail("CUDA device required for -m gpu tests")
     from transformer_head_scaled_gb300.build import build
     build()
+    oracle.build()
     return binding.load()
 
 
-def _inputs(B, h, n_q, L_max, seed):
-    w = Workload("na", B, h, n_q, L_max, 64, MASK_KEY_PADDING, "bf16", lens_lo=1, kind="decode")
+def _inputs(B, h, n_q, L_max, seed, d=64, zero_first=False):
+    w = Workload("na", B, h, n_q, L_max, d, MASK_KEY_PADDING, "bf16", lens_lo=1, kind="decode")
     q, k, v, lens = inputs.make_inputs(w, device="cuda", seeds=(seed, seed + 1, seed + 2, seed + 3))
+    if zero_first:
+        lens[0] = 0  # an empty cache: O = 0, LSE = -inf
     return w, q, k, v, lens
 
 
@@ -61,23 +68,49 @@ def _close(o, lse, o_ref, l_ref):
     assert (lse[fin] - l_ref[fin]).abs().max().item() <= 1e-3
 
 
-def test_noalloc_matches_workspace_entry_point_twice(lib):
-    # first a split cache (the partials go to the library's array), then a
-    # different problem that reuses the array after it
-    cases = [(1, 2, 2, 4096, 10), (3, 4, 1, 1000, 20)]
-    assert binding.decode_workspace_bytes(*cases[0][:4]) > 0
-    assert binding.decode_workspace_bytes(*cases[1][:4]) > 0
-    for B, h, n_q, L, seed in cases:
-        w, q, k, v, lens = _inputs(B, h, n_q, L, seed)
+def _close_oracle(w, q, k, v, lens, o, lse):
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, w.scale, MASK_KEY_PADDING, lens)
+    _close(o.cpu(), lse.cpu(), torch.from_numpy(o_ref), torch.from_numpy(l_ref))
+
+
+# B, h, n_q, L_max, seed, d, empty first cache
+CASES = [
+    (1, 2, 2, 4096, 10, 64, False),   # long split cache (TMA-fed kernel)
+    (3, 4, 1, 1000, 20, 64, True),    # a second problem over the array, one empty cache
+    (2, 8, 4, 8192, 40, 64, False),   # more partials than both calls before it
+    (2, 3, 2, 3000, 50, 128, True),   # plain-load kernel (d = 128), split, one empty cache
+    (2, 4, 1, 2500, 60, 32, False),   # plain-load kernel (d = 32), split
+]
+
+
+def test_noalloc_matches_oracle_and_workspace_entry_point(lib):
+    needs = []
+    for B, h, n_q, L, seed, d, zero in CASES:
+        need = binding.decode_workspace_bytes(B, h, n_q, L, d)
+        assert 0 < need <= binding.DECODE_NOALLOC_SCRATCH_BYTES
+        needs.append(need)
+        w, q, k, v, lens = _inputs(B, h, n_q, L, seed, d, zero)
         o_ref, l_ref = binding.attn_decode(q, k, v, lens, scale=w.scale)
         rc, o, lse = _noalloc(lib, w, q, k, v, lens)
         assert rc == binding.ATTN_OK, binding.status_string(rc)
         binding.check()
         _close(o, lse, o_ref, l_ref)
+        _close_oracle(w, q, k, v, lens, o, lse)
+    assert needs[2] > max(needs[0], needs[1])  # a later call uses more of the array
+
+
+def test_noalloc_unsplit_cache_needs_no_array(lib):
+    # one chunk per head: no partials, the array is not used
+    w, q, k, v, lens = _inputs(512, 8, 1, 256, 70, 64, True)
+    assert binding.decode_workspace_bytes(512, 8, 1, 256, 64) == 0
+    rc, o, lse = _noalloc(lib, w, q, k, v, lens)
+    assert rc == binding.ATTN_OK, binding.status_string(rc)
+    binding.check()
+    _close_oracle(w, q, k, v, lens, o, lse)
 
 
 def test_noalloc_refuses_sizes_beyond_its_array(lib):
-    # 600 heads of 8 queries, split in two: 600 * 2 * 8 partials of 264 bytes
+    # 600 heads of 8 queries over 1024-key caches: more partials than the array holds
     w, q, k, v, lens = _inputs(75, 8, 8, 1024, 30)
     need = binding.decode_workspace_bytes(75, 8, 8, 1024)
     assert need > binding.DECODE_NOALLOC_SCRATCH_BYTES

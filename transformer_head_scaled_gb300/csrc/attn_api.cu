@@ -551,7 +551,9 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   if (scratch_noalloc) {
     if (plan.workspace_bytes > ATTN_DECODE_NOALLOC_SCRATCH_BYTES)
       return ATTN_ERR_SCRATCH_TOO_SMALL;
-    if ((rc = scratch_on_device(&workspace)) != ATTN_OK) return rc;
+    // only a split cache writes partials: the array is not touched otherwise
+    workspace = nullptr;
+    if (plan.workspace_bytes > 0 && (rc = scratch_on_device(&workspace)) != ATTN_OK) return rc;
   } else if (plan.workspace_bytes > 0 && (workspace == nullptr ||
                                           workspace_bytes < plan.workspace_bytes ||
                                           !aligned16(workspace))) {
