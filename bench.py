@@ -171,8 +171,10 @@ def dist_env():
 
 
 def workload_desc(w: inputs.Workload) -> str:
-    mask = {0: "no mask", 1: "causal", 2: "key padding L~U[64,n_k]",
+    mask = {0: "no mask", 1: "causal", 2: f"key padding L~U[{w.lens_lo},n_k]",
             3: f"window i-{w.win_left}..i+{w.win_right}"}[w.mask]
+    if inputs.decode_window(w) is not None:
+        mask += f", keys L-1-{inputs.decode_window(w)}..L-1"
     return f"{w.name}: B={w.B} h={w.h} n_q={w.n_q} n_k={w.n_k} d_k=d_v={w.d} {w.dtype} {mask}"
 
 
@@ -187,7 +189,7 @@ def _row_flops(w: inputs.Workload, rows, lens) -> float:
         i = rows % w.n_q
         keys = np.maximum(np.minimum(w.n_k - 1, i + w.win_right) - np.maximum(0, i - w.win_left) + 1, 0)
     else:
-        keys = np.minimum(lens[(rows // w.n_q) // w.h], w.n_k)
+        keys = inputs.seen_keys(w, lens[(rows // w.n_q) // w.h])
     return float(4.0 * w.d * keys.sum())
 
 
@@ -195,6 +197,20 @@ def _oracle_rows(oracle, w, q, k, v, rows, kl, threads):
     if w.mask == inputs.MASK_BAND:
         return oracle.attn_band(q, k, v, w.scale, w.win_left, w.win_right, rows=rows,
                                 threads=threads)
+    win = inputs.decode_window(w)
+    if win is not None:
+        # restricted decoding step: batch entry b's rows against its window's
+        # slice of the cache
+        lens = np.asarray(kl.cpu())
+        per_b = w.h * w.n_q
+        for b in np.unique(rows // per_b):
+            L = int(min(max(lens[b], 0), w.n_k))
+            lo = max(0, L - 1 - win)
+            sub = rows[rows // per_b == b] - b * per_b
+            if L > lo:
+                oracle.attn_rows(q[b:b + 1], k[b:b + 1, :, lo:L], v[b:b + 1, :, lo:L], sub,
+                                 w.scale, inputs.MASK_NONE, threads=threads)
+        return None
     return oracle.attn_rows(q, k, v, rows, w.scale, w.mask, kl, threads=threads)
 
 
@@ -360,7 +376,8 @@ def run_ours(args, w):
     decode = w.kind == "decode"
     bwd = w.kind == "bwd"
     if decode:
-        ws_bytes = binding.decode_workspace_bytes(w.B, w.h, w.n_q, w.n_k, w.d)
+        ws_bytes = binding.decode_workspace_bytes(w.B, w.h, w.n_q, w.n_k, w.d,
+                                                  inputs.decode_window(w))
     elif bwd:
         ws_bytes = binding.bwd_workspace_bytes(w.B, w.h, w.n_q, w.d)
     else:
@@ -380,7 +397,11 @@ def run_ours(args, w):
                  lse.data_ptr(), *(t.data_ptr() for t in grads))
 
     def step():
-        if decode:
+        if decode and inputs.decode_window(w) is not None:
+            rc = binding.attn_decode_window_raw(*ptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale, klp,
+                                                inputs.decode_window(w), ws.data_ptr(), ws_bytes,
+                                                sptr)
+        elif decode:
             rc = binding.attn_decode_raw(*ptrs, w.B, w.h, w.n_q, w.n_k, w.d, w.scale, klp,
                                          ws.data_ptr(), ws_bytes, sptr)
         elif bwd and w.mask == inputs.MASK_BAND:
@@ -505,7 +526,8 @@ def run_e2e(args, w, q, k, v, kl, dev, stream, f32):
         0 if hkl is None else hkl.numel() * 4)
     d2h = ho.numel() * ho.element_size() + hl.numel() * 4
     sptr = int(stream.cuda_stream)
-    ws_bytes = (binding.decode_workspace_bytes(w.B, w.h, w.n_q, w.n_k, w.d)
+    ws_bytes = (binding.decode_workspace_bytes(w.B, w.h, w.n_q, w.n_k, w.d,
+                                               inputs.decode_window(w))
                 if w.kind == "decode" else 0)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     # the bf16 forward goes through attn_fwd_host: host buffers in and out, the
@@ -531,7 +553,14 @@ def run_e2e(args, w, q, k, v, kl, dev, stream, f32):
         dv.copy_(hv, non_blocking=True)
         if dkl is not None:
             dkl.copy_(hkl, non_blocking=True)
-        if w.kind == "decode":
+        if w.kind == "decode" and inputs.decode_window(w) is not None:
+            rc = binding.attn_decode_window_raw(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                                do.data_ptr(), dl.data_ptr(), w.B, w.h, w.n_q,
+                                                w.n_k, w.d, w.scale,
+                                                None if dkl is None else dkl.data_ptr(),
+                                                inputs.decode_window(w), ws.data_ptr(), ws_bytes,
+                                                sptr)
+        elif w.kind == "decode":
             rc = binding.attn_decode_raw(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                                          do.data_ptr(), dl.data_ptr(), w.B, w.h, w.n_q, w.n_k,
                                          w.d, w.scale, None if dkl is None else dkl.data_ptr(),

@@ -198,6 +198,30 @@ int attn_decode_strided(const void* q, const void* k_cache, const void* v_cache,
                         const int64_t* strides, float scale, const int* cache_lens,
                         void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
+/*
+ * attn_decode_window -- attn_decode with restricted self-attention
+ * ("Attention Is All You Need", section 4 and Table 1: each output position
+ * attends only to a neighbourhood of r positions around itself).  In a
+ * decoder the neighbourhood of the newest position holds only that position
+ * and earlier ones, so every query of (b, h) sees the cached keys j with
+ *   cache_lens[b] - 1 - window <= j < cache_lens[b]
+ * (the newest cached key and the `window` keys before it; attn_fwd_window
+ * with window_right = 0 at the last position).  Keys before the window are
+ * never read.  window >= 0 (ATTN_ERR_INVALID_ARG otherwise); a window of at
+ * least L_max - 1 gives attn_decode's result.  workspace_bytes must be at
+ * least attn_decode_window_workspace_bytes(B, h, n_q, L_max, d_k, window)
+ * (the cache is split by the window's length, not by L_max).  Other
+ * arguments, layouts and status codes as attn_decode.
+ */
+int attn_decode_window(const void* q, const void* k_cache, const void* v_cache, void* o,
+                       float* lse, int B, int h, int n_q, int L_max, int d_k, float scale,
+                       const int* cache_lens, int window, void* workspace,
+                       size_t workspace_bytes, struct CUstream_st* stream);
+
+/* Scratch bytes attn_decode_window needs (0 when no split is needed, for
+ * unsupported sizes or for window < 0). */
+size_t attn_decode_window_workspace_bytes(int B, int h, int n_q, int L_max, int d_k, int window);
+
 /* Size of the fixed scratch array behind attn_decode_noalloc (1 MiB). */
 #define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (1u << 20)
 

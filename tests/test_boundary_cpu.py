@@ -271,3 +271,17 @@ def test_decode_strided_arguments_rejected_on_host(lib):
     assert call(d=48) == binding.ATTN_ERR_UNSUPPORTED
     assert lib.attn_decode_strided(A, A, A, A, None, 1, 4, 1, 8, 64, None, 0.125, None, None, 0,
                                    None) == INV
+
+
+def test_decode_window_arguments_rejected_on_host(lib):
+    def call(q=A, window=16, d=64, n_q=1, lens=None):
+        return binding.attn_decode_window_raw(q, A, A, A, None, 1, 4, n_q, 8, d, 0.125, lens,
+                                              window, None, 0, None)
+    INV, UNS = binding.ATTN_ERR_INVALID_ARG, binding.ATTN_ERR_UNSUPPORTED
+    assert call(window=-1) == INV and call(window=-100) == INV
+    assert call(q=None) == INV
+    assert call(lens=A + 2) == INV
+    assert call(d=48) == UNS and call(n_q=9) == UNS
+    assert lib.attn_decode_window_workspace_bytes(1, 1, 1, 8, 64, -1) == 0
+    assert lib.attn_decode_window_workspace_bytes(1, 1, 9, 8, 64, 4) == 0   # unsupported sizes
+    assert lib.attn_decode_window_workspace_bytes(1, 1, 1, 8, 48, 4) == 0

@@ -31,8 +31,8 @@ DECODE_NOALLOC_SCRATCH_BYTES = 1 << 20
 # Every entry point declared in include/attn.h.
 EXPORTS = ("attn_fwd", "attn_fwd_f32", "attn_fwd_window", "attn_fwd_strided", "attn_fwd_host",
            "attn_fwd_host_buffer_bytes", "attn_decode", "attn_decode_strided",
-           "attn_decode_workspace_bytes",
-           "attn_decode_noalloc", "attn_bwd", "attn_bwd_window", "attn_bwd_strided",
+           "attn_decode_workspace_bytes", "attn_decode_window",
+           "attn_decode_window_workspace_bytes", "attn_decode_noalloc", "attn_bwd", "attn_bwd_window", "attn_bwd_strided",
            "attn_bwd_workspace_bytes",
            "attn_check", "attn_status_string",
            "attn_last_cuda_error", "attn_set_wait_limit_ns", "attn_launch_count",
@@ -81,6 +81,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                             vp]
         lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+        lib.attn_decode_window.restype = i32
+        lib.attn_decode_window.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp,
+                                           i32, vp, ctypes.c_size_t, vp]
+        lib.attn_decode_window_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_decode_window_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.attn_bwd.restype = i32
         lib.attn_bwd.argtypes = [vp] * 9 + [i32] * 5 + [f32, i32, vp, vp, ctypes.c_size_t, vp]
         lib.attn_decode_strided.restype = i32
@@ -336,8 +341,12 @@ def attn_fwd_f32(q, k, v, **kw):
     return attn_fwd(q, k, v, **kw)
 
 
-def decode_workspace_bytes(B: int, h: int, n_q: int, L_max: int, d: int = 64) -> int:
-    """Scratch bytes attn_decode needs on the current device (0: none)."""
+def decode_workspace_bytes(B: int, h: int, n_q: int, L_max: int, d: int = 64,
+                           window: int | None = None) -> int:
+    """Scratch bytes attn_decode (attn_decode_window when `window` is given)
+    needs on the current device (0: none)."""
+    if window is not None:
+        return int(load().attn_decode_window_workspace_bytes(B, h, n_q, L_max, d, int(window)))
     return int(load().attn_decode_workspace_bytes(B, h, n_q, L_max, d))
 
 
@@ -346,6 +355,14 @@ def attn_decode_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, L_max, d, sc
     """The C call itself, on raw device pointers; returns the status code."""
     return load().attn_decode(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, L_max, d,
                               float(scale), lens_ptr, ws_ptr, int(ws_bytes), stream_ptr)
+
+
+def attn_decode_window_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, L_max, d, scale,
+                           lens_ptr, window, ws_ptr, ws_bytes, stream_ptr) -> int:
+    """attn_decode_window on raw device pointers; returns the status code."""
+    return load().attn_decode_window(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, L_max, d,
+                                     float(scale), lens_ptr, int(window), ws_ptr, int(ws_bytes),
+                                     stream_ptr)
 
 
 def attn_decode_strided_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, h, n_q, L_max, d, strides,
@@ -400,10 +417,12 @@ def attn_decode_strided(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
 def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                 cache_lens: torch.Tensor | None = None, scale: float | None = None,
                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-                workspace: torch.Tensor | None = None, with_lse: bool = True, stream=None):
+                workspace: torch.Tensor | None = None, with_lse: bool = True, stream=None,
+                window: int | None = None):
     """n_q <= 8 new queries q [B,h,n_q,d] against bf16 caches [B,h,L_max,d];
-    query i sees the first cache_lens[b] keys (all L_max when None).
-    Returns (o, lse)."""
+    query i sees the first cache_lens[b] keys (all L_max when None), or with
+    `window` (attn_decode_window) only keys cache_lens[b]-1-window ..
+    cache_lens[b]-1.  Returns (o, lse)."""
     for t in (q, k_cache, v_cache):
         if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
             raise ValueError("q and the caches must be contiguous bf16 CUDA [B, h, n, d] tensors")
@@ -420,15 +439,20 @@ def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         out = torch.empty((B, h, n_q, d), dtype=q.dtype, device=q.device)
     if lse is None and with_lse:
         lse = torch.empty((B, h, n_q), dtype=torch.float32, device=q.device)
-    need = decode_workspace_bytes(B, h, n_q, L_max, d)
+    need = decode_workspace_bytes(B, h, n_q, L_max, d, window)
     if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = attn_decode_raw(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), B, h, n_q,
-                         L_max, d, scale, _ptr(cache_lens), _ptr(workspace), ws_bytes,
-                         _stream_ptr(stream))
+    if window is None:
+        rc = attn_decode_raw(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), B, h,
+                             n_q, L_max, d, scale, _ptr(cache_lens), _ptr(workspace), ws_bytes,
+                             _stream_ptr(stream))
+    else:
+        rc = attn_decode_window_raw(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse),
+                                    B, h, n_q, L_max, d, scale, _ptr(cache_lens), window,
+                                    _ptr(workspace), ws_bytes, _stream_ptr(stream))
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_decode")
+        raise AttnError(rc, "attn_decode" if window is None else "attn_decode_window")
     return out, lse
 
 

@@ -528,17 +528,25 @@ size_t attn_decode_workspace_bytes(int B, int h, int n_q, int L_max, int d_k) {
   return decode_plan(B, h, n_q, L_max, d_k, di->num_sms).workspace_bytes;
 }
 
+size_t attn_decode_window_workspace_bytes(int B, int h, int n_q, int L_max, int d_k, int window) {
+  if (window < 0) return 0;
+  // the splits cover the window's keys only
+  return attn_decode_workspace_bytes(B, h, n_q, window < L_max ? window + 1 : L_max, d_k);
+}
+
 }  // extern "C"
 
 namespace attn {
 namespace {
 // st: strides of q, k_cache, v_cache, o, or null for contiguous tensors.
 // scratch_noalloc: take the partials' space from the library's own array
-// instead of the caller's workspace.
+// instead of the caller's workspace.  window: restricted self-attention
+// (keys [len - 1 - window, len)), or -1 for all cached keys.
 static int decode_impl(const void* q, const void* k_cache, const void* v_cache, void* o,
                        float* lse, int B, int h, int n_q, int L_max, int d_k, const Strides* st,
                        float scale, const int* cache_lens, void* workspace,
-                       size_t workspace_bytes, bool scratch_noalloc, struct CUstream_st* stream) {
+                       size_t workspace_bytes, bool scratch_noalloc, struct CUstream_st* stream,
+                       int window = -1) {
   int rc = check_common(q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, scale,
                         ATTN_MASK_NONE, nullptr, 2);
   if (rc != ATTN_OK) return rc;
@@ -547,7 +555,9 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
   if (static_cast<long long>(B) * h > 65535) return ATTN_ERR_UNSUPPORTED;  // grid.y
   DeviceInfo* di = nullptr;
   if ((rc = device_info(&di)) != ATTN_OK) return rc;
-  const DecodePlan plan = decode_plan(B, h, n_q, L_max, d_k, di->num_sms);
+  // the most keys one query sees: what the cache is split by
+  const int seen = window >= 0 && window < L_max ? window + 1 : L_max;
+  const DecodePlan plan = decode_plan(B, h, n_q, seen, d_k, di->num_sms);
   if (scratch_noalloc) {
     if (plan.workspace_bytes > ATTN_DECODE_NOALLOC_SCRATCH_BYTES)
       return ATTN_ERR_SCRATCH_TOO_SMALL;
@@ -566,7 +576,7 @@ static int decode_impl(const void* q, const void* k_cache, const void* v_cache, 
       (rc = encode_decode_maps(maps, k_cache, v_cache, d_k, L_max, B, h, sk, sv)) != ATTN_OK)
     return rc;
   DecodeProblem pb{q,  k_cache, v_cache, o,          lse, B,  h,  n_q, L_max,
-                   d_k, scale,  cache_lens, sq, sk, sv, so};
+                   d_k, scale,  cache_lens, sq, sk, sv, so, window};
   cudaError_t e = launch_decode(pb, maps, plan, static_cast<float*>(workspace),
                                 make_ctx(*di, stream));
   if (e != cudaSuccess) return cuda_fail(e);
@@ -583,6 +593,15 @@ int attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o
                 void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
   return decode_impl(q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, nullptr, scale,
                      cache_lens, workspace, workspace_bytes, false, stream);
+}
+
+int attn_decode_window(const void* q, const void* k_cache, const void* v_cache, void* o,
+                       float* lse, int B, int h, int n_q, int L_max, int d_k, float scale,
+                       const int* cache_lens, int window, void* workspace,
+                       size_t workspace_bytes, struct CUstream_st* stream) {
+  if (window < 0) return ATTN_ERR_INVALID_ARG;
+  return decode_impl(q, k_cache, v_cache, o, lse, B, h, n_q, L_max, d_k, nullptr, scale,
+                     cache_lens, workspace, workspace_bytes, false, stream, window);
 }
 
 int attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o,

@@ -71,10 +71,20 @@ struct DecParams {
   float* lse;
   float* part;  // workspace: [B*h][splits][n_q][DK + 2] (m, l, O), or null
   int H, BH, n_q, L_max, splits, chunk;
+  int win;  // restricted self-attention: a query sees keys [L - 1 - win, L); -1: all keys
   float scale_log2;
   uint64_t limit_ns;
   int* status;
 };
+
+// Keys [begin, end) of split sp of a cache filled to L: the splits cover the
+// keys the queries see, [0, L), or [L - 1 - win, L) with a window.
+__device__ __forceinline__ void chunk_keys(const DecParams& p, int L, int sp, int& begin,
+                                           int& end) {
+  const int lo = p.win >= 0 ? max(L - 1 - p.win, 0) : 0;
+  begin = lo + sp * p.chunk;
+  end = min(L, begin + p.chunk);
+}
 
 // Element offset of row i of head bh (= b * H + h) in a strided tensor.
 __device__ __forceinline__ long long row_off(const RowStrides& s, int bh, int H, int i) {
@@ -115,8 +125,7 @@ __global__ void __launch_bounds__(THREADS, 3)
     bh = u / p.splits;
     int L = p.L_max;
     if (p.cache_lens != nullptr) L = min(max(__ldg(p.cache_lens + bh / p.H), 0), p.L_max);
-    begin = (u % p.splits) * p.chunk;
-    end = min(L, begin + p.chunk);
+    chunk_keys(p, L, u % p.splits, begin, end);
   };
 
   if (threadIdx.x == 0) {
@@ -139,8 +148,9 @@ __global__ void __launch_bounds__(THREADS, 3)
     const int maxk = max(1, min(p.chunk, p.L_max));
     auto bucket_of = [&](int e) {  // key-count class of pair e (0: no key)
       const int L = min(max(__ldg(p.cache_lens + e / p.splits), 0), p.L_max);
-      const int begin = (e % p.splits) * p.chunk;
-      const int keys = min(L, begin + p.chunk) - begin;
+      int begin, end;
+      chunk_keys(p, L, e % p.splits, begin, end);
+      const int keys = end - begin;
       return keys <= 0 ? 0 : 1 + min(NBUCKET - 2, ((keys - 1) * (NBUCKET - 1)) / maxk);
     };
     for (int i = threadIdx.x; i < NBUCKET; i += THREADS) sm.sort.count[i] = 0;
@@ -460,8 +470,8 @@ __global__ void __launch_bounds__(THREADS)
   const int bh = u / p.splits;
   int L = p.L_max;
   if (p.cache_lens != nullptr) L = min(max(__ldg(p.cache_lens + bh / p.H), 0), p.L_max);
-  const int begin = (u % p.splits) * p.chunk;
-  const int end = min(L, begin + p.chunk);
+  int begin, end;
+  chunk_keys(p, L, u % p.splits, begin, end);
   for (int e = threadIdx.x; e < NQ * D; e += THREADS)
     sq[e / D][e % D] =
         __bfloat162float(p.q[row_off(p.sq, bh, p.H, e / D) + e % D]) * p.scale_log2;
@@ -713,6 +723,7 @@ cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap* maps, cons
   p.L_max = pb.L_max;
   p.splits = plan.splits;
   p.chunk = plan.chunk;
+  p.win = pb.window;
   p.sq = pb.sq;
   p.sk = pb.sk;
   p.sv = pb.sv;

@@ -65,6 +65,7 @@ struct DecodeProblem {
   float scale;
   const int* cache_lens;  // device int32[B] or null (all L_max valid)
   RowStrides sq, sk, sv, so;  // element strides (batch entry, head, row) of q, k, v, o
+  int window = -1;  // restricted self-attention: keys [len - 1 - window, len); -1: all keys
 };
 
 // How the cache of each head is split across CTAs; workspace_bytes = 0 when
@@ -74,6 +75,7 @@ struct DecodePlan {
   int chunk;  // keys per split, a multiple of the 128-key tile
   size_t workspace_bytes;
 };
+// L_max: the most keys one query sees (the cache length, or the window's).
 DecodePlan decode_plan(int B, int H, int n_q, int L_max, int d, int num_sms);
 // maps[0..3] (d = 64; unused for the other head sizes, whose kernel reads the
 // cache with plain loads): K cache, V cache as 4-D (64, L_max, H, B) bf16 with

@@ -52,7 +52,7 @@ class Workload:
     lens_lo: int = 64
     kind: str = "fwd"  # "fwd": fused forward; "decode": few queries against a cache;
     #                    "bwd": gradients of the forward
-    win_left: int = 0   # MASK_BAND only
+    win_left: int = 0   # MASK_BAND; for kind "decode", > 0: attn_decode_window's window
     win_right: int = 0
     note: str = field(default="", compare=False)
 
@@ -90,6 +90,9 @@ WORKLOADS = {
                             note="big model, 8 sentences x beam 4, cache up to 4096"),
     # The decoding step of the base model split into other head counts
     # ("Attention Is All You Need", Table 3, rows (A)): the same cache bytes.
+    "decode_long_window": Workload("decode_long_window", 32, 16, 1, 4096, 64, MASK_KEY_PADDING,
+                                   "bf16", lens_lo=2048, kind="decode", win_left=1023,
+                                   note="decode_long, restricted to the newest 1024 positions"),
     "decode_beam_h4_d128": Workload("decode_beam_h4_d128", 256, 4, 1, 512, 128, MASK_KEY_PADDING,
                                     "bf16", kind="decode",
                                     note="decode_beam with 4 heads of 128"),
@@ -177,11 +180,26 @@ def products(w: Workload) -> float:
     return 5.0 if w.kind == "bwd" else 2.0
 
 
+def decode_window(w: Workload):
+    """The window of a restricted decoding step (keys len-1-window .. len-1),
+    or None for attention over the whole cache."""
+    return w.win_left if w.kind == "decode" and w.win_left > 0 else None
+
+
+def seen_keys(w: Workload, lens):
+    """Keys each batch entry's queries see in a decoding step: the filled
+    cache, or its newest window + 1 positions."""
+    seen = np.minimum(np.asarray(lens), w.n_k)
+    win = decode_window(w)
+    return seen if win is None else np.minimum(seen, win + 1)
+
+
 def flops(w: Workload, key_lens=None) -> float:
     """Nominal FLOPs of one pass: 2*n_q*n_k*d per contraction and head
     (forward 4*B*h*n_q*n_k*d, backward 2.5 times that), halved for the causal
-    mask."""
-    f = 2.0 * products(w) * w.B * w.h * w.n_q * w.n_k * w.d
+    mask; a restricted decoding step counts window + 1 keys."""
+    n_k = w.n_k if decode_window(w) is None else min(w.n_k, decode_window(w) + 1)
+    f = 2.0 * products(w) * w.B * w.h * w.n_q * n_k * w.d
     if w.mask == MASK_CAUSAL:
         f *= 0.5
     if w.mask == MASK_BAND:
@@ -211,14 +229,15 @@ def algorithmic_flops(w: Workload, key_lens=None) -> float:
         return 2.0 * products(w) * w.B * w.h * pairs * w.d
     if w.mask == MASK_KEY_PADDING:
         lens = np.asarray(key_lens.cpu() if hasattr(key_lens, "cpu") else key_lens)
-        return 2.0 * products(w) * w.h * w.n_q * float(np.minimum(lens, w.n_k).sum()) * w.d
+        return 2.0 * products(w) * w.h * w.n_q * float(seen_keys(w, lens).sum()) * w.d
     return flops(w)
 
 
 def hbm_bytes(w: Workload, key_lens=None) -> float:
     """Compulsory HBM bytes of one forward pass: Q, K, V read once, O written
     once, LSE (float32) written once; the n_q x n_k scores never leave the chip.
-    For a decoding step only the filled part of the caches is read.  The
+    For a decoding step only the filled part of the caches is read (of a
+    restricted step, only its window).  The
     backward reads Q, K, V, O, dO and LSE and writes dQ, dK, dV."""
     es = 2 if w.dtype == "bf16" else 4
     if w.kind == "bwd":
@@ -227,7 +246,7 @@ def hbm_bytes(w: Workload, key_lens=None) -> float:
     qo = 2 * w.B * w.h * w.n_q * w.d * es
     if w.kind == "decode" and key_lens is not None:
         lens = np.asarray(key_lens.cpu() if hasattr(key_lens, "cpu") else key_lens)
-        kv = 2 * w.h * float(np.minimum(lens, w.n_k).sum()) * w.d * es
+        kv = 2 * w.h * float(seen_keys(w, lens).sum()) * w.d * es
     else:
         kv = 2 * w.B * w.h * w.n_k * w.d * es
     return float(qo + kv + 4 * w.B * w.h * w.n_q)
