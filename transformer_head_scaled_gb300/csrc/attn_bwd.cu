@@ -355,6 +355,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  // Launched as a dependent of the preprocess kernel (which writes the
+  // constant tiles and zeroes the dQ accumulator): everything above overlaps
+  // its tail, nothing below runs before it has completed.
+  grid_dependency_wait();
 
   if (warp == LOAD_WARP) {
     // -------------------------------------------------------------- producer
@@ -834,6 +838,9 @@ __global__ void __launch_bounds__(256)
                         const float* __restrict__ lse, uint8_t* __restrict__ cst,
                         float* __restrict__ dq_acc, int H, int n_q, int num_qt, float inv_scale,
                         long long rows, RowStrides so, RowStrides sdo) {
+  // the main kernel may start launching now: it waits for this grid to
+  // complete before it reads the constants or adds into dq_acc
+  grid_launch_dependents();
   constexpr int TPR = D / 8;  // threads a row
   const long long row = static_cast<long long>(blockIdx.x) * (256 / TPR) + threadIdx.x / TPR;
   const int sub = threadIdx.x % TPR;
@@ -889,6 +896,7 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     attn_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
                        float scale, long long n8, int d8, int H, int n_q, RowStrides sdq) {
+  grid_dependency_wait();  // the main kernel's additions into dq_acc are complete
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n8) return;
   const long long r = i / d8;  // row (b * H + hh) * n_q + qi of the accumulator
@@ -963,19 +971,21 @@ cudaError_t launch_bwd_d(const BwdProblem& pb, const CUtensorMap* maps, void* wo
                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int grid = p.num_items < ctx.num_sms ? p.num_items : ctx.num_sms;
-  if (band)
-    attn_bwd_tc_kernel<true, D><<<grid, NUM_THREADS, smem, ctx.stream>>>(
-        maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], p);
-  else
-    attn_bwd_tc_kernel<false, D><<<grid, NUM_THREADS, smem, ctx.stream>>>(
-        maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], p);
-  err = cudaGetLastError();
+  // the main and the dQ kernels start while their predecessor drains
+  // (programmatic dependent launch; each waits for it before reading its output)
+  err = band ? launch_dependent(attn_bwd_tc_kernel<true, D>, dim3(grid), dim3(NUM_THREADS), smem,
+                                ctx.stream, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+                                maps[6], p)
+             : launch_dependent(attn_bwd_tc_kernel<false, D>, dim3(grid), dim3(NUM_THREADS), smem,
+                                ctx.stream, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+                                maps[6], p);
   if (err != cudaSuccess) return err;
 
   const long long n8 = bh * pb.n_q * (D / 8);
-  attn_bwd_dq_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, ctx.stream>>>(
-      dq_acc, static_cast<__nv_bfloat16*>(pb.dq), pb.scale, n8, D / 8, pb.H, pb.n_q, pb.sdq);
-  return cudaGetLastError();
+  return launch_dependent(attn_bwd_dq_kernel, dim3(static_cast<unsigned>((n8 + 255) / 256)),
+                          dim3(256), 0, ctx.stream, static_cast<const float*>(dq_acc),
+                          static_cast<__nv_bfloat16*>(pb.dq), pb.scale, n8, D / 8, pb.H, pb.n_q,
+                          pb.sdq);
 }
 
 }  // namespace

@@ -622,6 +622,7 @@ __global__ void __launch_bounds__(128)
     attn_decode_combine_kernel(const float* __restrict__ part, __nv_bfloat16* __restrict__ o,
                                float* __restrict__ lse, int rows, int n_q, int splits, int H,
                                RowStrides so) {
+  grid_dependency_wait();  // the split kernel's partial results are complete
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);  // (bh * n_q + qi)
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -755,17 +756,19 @@ cudaError_t launch_decode(const DecodeProblem& pb, const CUtensorMap* maps, cons
   if (err != cudaSuccess || plan.splits == 1) return err;
   const int rows = BH * pb.n_q;
   const unsigned blocks = static_cast<unsigned>((rows + 3) / 4);
+  // the merge starts while the split kernel drains (programmatic dependent
+  // launch; it waits for the split kernel's partials before reading them)
+  auto merge = [&](auto kernel) {
+    return launch_dependent(kernel, dim3(blocks), dim3(128), 0, ctx.stream,
+                            static_cast<const float*>(workspace), p.o, p.lse, rows, pb.n_q,
+                            plan.splits, pb.H, pb.so);
+  };
   switch (pb.d) {
-    case 16: attn_decode_combine_kernel<16><<<blocks, 128, 0, ctx.stream>>>(
-                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits, pb.H, pb.so); break;
-    case 32: attn_decode_combine_kernel<32><<<blocks, 128, 0, ctx.stream>>>(
-                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits, pb.H, pb.so); break;
-    case 64: attn_decode_combine_kernel<64><<<blocks, 128, 0, ctx.stream>>>(
-                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits, pb.H, pb.so); break;
-    default: attn_decode_combine_kernel<128><<<blocks, 128, 0, ctx.stream>>>(
-                 workspace, p.o, p.lse, rows, pb.n_q, plan.splits, pb.H, pb.so); break;
+    case 16: return merge(attn_decode_combine_kernel<16>);
+    case 32: return merge(attn_decode_combine_kernel<32>);
+    case 64: return merge(attn_decode_combine_kernel<64>);
+    default: return merge(attn_decode_combine_kernel<128>);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace attn

@@ -35,6 +35,27 @@ struct LaunchCtx {
   cudaStream_t stream;
 };
 
+// Launches `kernel` with programmatic stream serialization: it may start (and
+// run its prologue) while the previous kernel on the stream drains, so the
+// kernel must call ptx::grid_dependency_wait() before it reads anything the
+// previous kernel writes.  Used only for the second and later kernels of one
+// library call, whose predecessor on the stream is always that call's own.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                   cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // tcgen05 bf16 path, d in {16, 32, 64, 128}.  The tensor maps describe Q, K,
 // V and O as 3-D (d, n, B*H) bf16 tensors with a (min(d, 64), rows, 1) box
 // in the widest swizzle a box row fits (128, 64 or 32 bytes); rows = 128 for
