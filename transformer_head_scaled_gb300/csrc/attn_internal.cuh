@@ -35,9 +35,24 @@ struct LaunchCtx {
   cudaStream_t stream;
 };
 
+// Programmatic dependent launch (PTX griddepcontrol): a kernel launched with
+// the programmatic stream serialization attribute may start while the kernel
+// before it on the stream is still running.  It must pass this wait before it
+// touches anything that kernel writes: the wait returns once that grid has
+// completed and its memory operations are visible (at once for a kernel
+// launched without the attribute).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel on the stream start launching before this grid ends
+// (its CTAs still wait in grid_dependency_wait for this grid to complete).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Launches `kernel` with programmatic stream serialization: it may start (and
 // run its prologue) while the previous kernel on the stream drains, so the
-// kernel must call ptx::grid_dependency_wait() before it reads anything the
+// kernel must call grid_dependency_wait() before it reads anything the
 // previous kernel writes.  Used only for the second and later kernels of one
 // library call, whose predecessor on the stream is always that call's own.
 template <typename... KArgs, typename... Args>

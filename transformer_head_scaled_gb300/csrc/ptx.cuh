@@ -351,23 +351,6 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// ------------------------------------------------------------------ grid dependencies
-
-// Programmatic dependent launch (PTX griddepcontrol): a kernel launched with
-// the programmatic stream serialization attribute may start while the kernel
-// before it on the stream is still running.  It must pass this wait before it
-// touches anything that kernel writes: the wait returns once that grid has
-// completed and its memory operations are visible (at once for a kernel
-// launched without the attribute).
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-// Lets the next kernel on the stream start launching before this grid ends
-// (its CTAs still wait in grid_dependency_wait for this grid to complete).
-__device__ __forceinline__ void grid_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // ------------------------------------------------------------------ math
 
 // 2^x on the special-function unit (PTX ex2.approx.ftz.f32).
