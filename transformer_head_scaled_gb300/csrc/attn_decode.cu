@@ -46,12 +46,17 @@ constexpr int SORT_MAX = 1024;
 constexpr int SCHED_MAX = 32;
 constexpr int NBUCKET = 64;  // key-count classes of that ordering
 
+// Queries and per-warp partials are double-buffered by the parity of a
+// unit's position in the CTA's list, so that one barrier per unit suffices.
+template <int NQ>
 struct __align__(1024) DecSmem {
   uint8_t k[DSTAGES][TILE_BYTES];
   uint8_t v[DSTAGES][TILE_BYTES];
   union {
-    float q[kDecodeMaxQueries][DK];                // queries, pre-scaled by scale*log2(e)
-    float red[NWARPS][kDecodeMaxQueries][DK + 2];  // per-warp partials, after the tiles
+    struct {
+      float q[2][NQ][DK];                // queries, pre-scaled by scale*log2(e)
+      float red[2][NWARPS][NQ][DK + 2];  // per-warp partials, after the tiles
+    } b;
     struct {
       int count[NBUCKET];  // (batch entry, split) pairs per key-count class
       int first[NBUCKET];  // sorted position of each class's first pair
@@ -105,19 +110,24 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Resident CTAs per SM: three while their shared memory fits (228 KB per SM,
+// 1 KB of it reserved per CTA, 1 KB of alignment slack each), else two.
+template <int NQ>
+constexpr int split_ctas() { return 3 * (sizeof(DecSmem<NQ>) + 2048) <= 233472 ? 3 : 2; }
+
 // Persistent: CTA c processes the work units c, c + gridDim.x, ... (a unit
 // is one chunk of one head's cache); thread 0 keeps the TMA ring DSTAGES
 // tiles ahead across unit boundaries, so the next head's first tiles are in
 // flight while the current one is finished.
 template <int NQ>
-__global__ void __launch_bounds__(THREADS, 3)
+__global__ void __launch_bounds__(THREADS, split_ctas<NQ>())
     attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
                              const __grid_constant__ CUtensorMap tmv,
                              const __grid_constant__ CUtensorMap tmk_tail,
                              const __grid_constant__ CUtensorMap tmv_tail, const DecParams p) {
   extern __shared__ uint8_t smem_raw[];
-  DecSmem& sm = *reinterpret_cast<DecSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                            ~static_cast<uintptr_t>(1023));
+  DecSmem<NQ>& sm = *reinterpret_cast<DecSmem<NQ>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int units = p.BH * p.splits;
   // keys [begin, end) of unit u's chunk
@@ -281,24 +291,29 @@ __global__ void __launch_bounds__(THREADS, 3)
     }
   };
   float qv[QPT];
+  // the first unit's queries into buffer 0 (the schedule above is done with
+  // the shared space: the barrier after it)
+  auto store_q = [&](int buf) {
+#pragma unroll
+    for (int i = 0; i < QPT; ++i) {
+      const int e = threadIdx.x + i * THREADS;
+      if (e < NQ * DK) sm.b.q[buf][e / DK][e % DK] = qv[i] * p.scale_log2;
+    }
+  };
   load_q(unit_at(0), qv);
+  store_q(0);
+  __syncthreads();
 
   uint32_t consumed = 0;
   bool ok = true;
   const int r = warp * 32 + lane;  // this lane's key row inside a tile
   for (int ui = 0; ui < n_units && ok; ++ui) {
     const int u = unit_at(ui);
+    const int qbuf = ui & 1;  // this unit's query and partial buffers
     int bh, begin, end;
     unit_keys(u, bh, begin, end);
     const int ntiles = end > begin ? (end - begin + KT - 1) / KT : 0;
-    __syncthreads();  // the previous unit's merge has read sm.red and sm.q
-#pragma unroll
-    for (int i = 0; i < QPT; ++i) {
-      const int e = threadIdx.x + i * THREADS;
-      if (e < NQ * DK) sm.q[e / DK][e % DK] = qv[i] * p.scale_log2;
-    }
-    __syncthreads();
-    load_q(unit_at(ui + 1), qv);  // the next unit's queries, consumed after this unit
+    load_q(unit_at(ui + 1), qv);  // the next unit's queries, stored after this unit's tiles
 
     float m[NQ], l[NQ], o0[NQ], o1[NQ];  // this warp's running state per query
 #pragma unroll
@@ -321,8 +336,8 @@ __global__ void __launch_bounds__(THREADS, 3)
                              bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
 #pragma unroll
         for (int qi = 0; qi < NQ; ++qi) {
-          const float4 qa = *reinterpret_cast<const float4*>(&sm.q[qi][c * 8]);
-          const float4 qb = *reinterpret_cast<const float4*>(&sm.q[qi][c * 8 + 4]);
+          const float4 qa = *reinterpret_cast<const float4*>(&sm.b.q[qbuf][qi][c * 8]);
+          const float4 qb = *reinterpret_cast<const float4*>(&sm.b.q[qbuf][qi][c * 8 + 4]);
           s[qi] = fmaf(qa.x, kf[0], s[qi]);
           s1[qi] = fmaf(qa.y, kf[1], s1[qi]);
           s2[qi] = fmaf(qa.z, kf[2], s2[qi]);
@@ -387,17 +402,19 @@ __global__ void __launch_bounds__(THREADS, 3)
     }
     if (!ok) break;
 
-    // ---- merge the four warps' states: lane sums, then across warps in smem
-    // (sm.red shares its space with sm.q: every warp is done with q first)
-    __syncthreads();
+    // ---- merge the four warps' states: lane sums, then across warps in smem.
+    // The other buffers were last read before the previous unit's barrier,
+    // which every warp has passed: the next unit's queries and this unit's
+    // partials go there now, and one barrier publishes both.
+    store_q(qbuf ^ 1);
 #pragma unroll
     for (int qi = 0; qi < NQ; ++qi) {
       const float lw = warp_sum(l[qi]);
-      sm.red[warp][qi][2 * lane] = o0[qi];
-      sm.red[warp][qi][2 * lane + 1] = o1[qi];
+      sm.b.red[qbuf][warp][qi][2 * lane] = o0[qi];
+      sm.b.red[qbuf][warp][qi][2 * lane + 1] = o1[qi];
       if (lane == 0) {
-        sm.red[warp][qi][DK] = m[qi];
-        sm.red[warp][qi][DK + 1] = lw;
+        sm.b.red[qbuf][warp][qi][DK] = m[qi];
+        sm.b.red[qbuf][warp][qi][DK + 1] = lw;
       }
     }
     __syncthreads();
@@ -405,15 +422,15 @@ __global__ void __launch_bounds__(THREADS, 3)
     for (int qi = warp; qi < NQ; qi += NWARPS) {
       float mm = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < NWARPS; ++w) mm = fmaxf(mm, sm.red[w][qi][DK]);
+      for (int w = 0; w < NWARPS; ++w) mm = fmaxf(mm, sm.b.red[qbuf][w][qi][DK]);
       const float base = mm == -INFINITY ? 0.f : mm;
       float ll = 0.f, a0 = 0.f, a1 = 0.f;
 #pragma unroll
       for (int w = 0; w < NWARPS; ++w) {
-        const float f = ex2(sm.red[w][qi][DK] - base);
-        ll += f * sm.red[w][qi][DK + 1];
-        a0 += f * sm.red[w][qi][2 * lane];
-        a1 += f * sm.red[w][qi][2 * lane + 1];
+        const float f = ex2(sm.b.red[qbuf][w][qi][DK] - base);
+        ll += f * sm.b.red[qbuf][w][qi][DK + 1];
+        a0 += f * sm.b.red[qbuf][w][qi][2 * lane];
+        a1 += f * sm.b.red[qbuf][w][qi][2 * lane + 1];
       }
       const size_t row = static_cast<size_t>(bh) * NQ + qi;
       if (p.splits == 1) {
@@ -653,13 +670,14 @@ __global__ void __launch_bounds__(128)
 template <int NQ>
 cudaError_t launch_split(const CUtensorMap* maps, const DecParams& p, int BH, int num_sms,
                          cudaStream_t stream) {
-  const size_t smem = sizeof(DecSmem) + 1024;
+  const size_t smem = sizeof(DecSmem<NQ>) + 1024;
   cudaError_t err = cudaFuncSetAttribute(attn_decode_split_kernel<NQ>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int units = p.splits * BH;
-  const int grid = units < 3 * num_sms ? units : 3 * num_sms;  // three resident CTAs per SM
+  const int per_sm = split_ctas<NQ>();  // resident CTAs per SM
+  const int grid = units < per_sm * num_sms ? units : per_sm * num_sms;
   attn_decode_split_kernel<NQ><<<grid, THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3],
                                                                   p);
   return cudaGetLastError();
