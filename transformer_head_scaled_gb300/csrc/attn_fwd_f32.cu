@@ -4,99 +4,186 @@
 // Same operation as the tensor-core path (eq. (1) of "Attention Is All You
 // Need", section 3.2.1, masks of section 3.2.3), for float32 tensors where
 // the tensor-core path's bf16 rounding would not meet a 1e-4 tolerance.  One
-// thread owns one query row; K/V tiles of 32 keys are staged in shared
-// memory and consumed with a streaming softmax in base 2 (scale*log2(e)
-// folded into the scores): per tile, the new running max rescales the
-// accumulator once, then each key adds 2^(x - m) * v.
+// warp owns one query row and walks its visible keys 32 at a time with a
+// streaming softmax in base 2 (scale*log2(e) folded into the query): for the
+// scores lane l takes key l of the group (its row read with 16-byte loads,
+// the query from shared memory); for P V, LPK = min(d, 32) lanes share one
+// value row, each holding d / LPK consecutive output columns, 32 / LPK keys
+// at a time.  The 8 warps of a CTA (8 query rows of one head) share the K/V
+// tiles, staged in shared memory with asynchronous copies one tile ahead.
 #include "attn_internal.cuh"
 
 namespace attn {
 namespace {
 
-constexpr int ROWS_PER_CTA = 64;
-constexpr int KEYS_PER_TILE = 32;
+constexpr int ROWS_PER_CTA = 8;  // one warp per query row
+constexpr float LN2 = 0.693147180559945309f;
+
+// 16-byte asynchronous copy global -> shared (zero-filled when !in: no byte
+// is read then), so that a whole tile's copies are in flight at once.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool in) {
+  const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(gmem),
+               "r"(in ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+constexpr int KT = 32;  // keys per tile (one per lane for the scores)
+
+// Shared memory of one CTA: K and V tiles (double-buffered), rows padded by
+// 16 bytes so that the lanes' 16-byte reads of 32 different K rows spread
+// over the banks; each warp's query row.
+template <int D>
+struct F32Smem {
+  static constexpr int RS = D + 4;  // row stride in floats
+  float k[2][KT][RS];
+  float v[2][KT][RS];
+  float q[ROWS_PER_CTA][D];
+};
 
 template <int D>
-__global__ void __launch_bounds__(ROWS_PER_CTA)
+__global__ void __launch_bounds__(ROWS_PER_CTA * 32)
     attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                         const float* __restrict__ v, float* __restrict__ o,
                         float* __restrict__ lse, int H, int n_q, int n_k, float scale_log2,
                         int mask, const int* __restrict__ key_lens) {
-  __shared__ float ks[KEYS_PER_TILE][D];
-  __shared__ float vs[KEYS_PER_TILE][D];
+  constexpr int LPK = D < 32 ? D : 32;  // lanes per value row in P V
+  constexpr int KPI = 32 / LPK;         // keys per P V step
+  constexpr int DPL = D / LPK;          // output columns per lane
+  extern __shared__ __align__(16) uint8_t f32_smem[];
+  F32Smem<D>& sm = *reinterpret_cast<F32Smem<D>*>(f32_smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
   const int row0 = blockIdx.x * ROWS_PER_CTA;
-  const int row = row0 + threadIdx.x;
-  const bool valid = row < n_q;
+  const int row = row0 + warp;
+  const bool live = row < n_q;  // rows past n_q take part in the copies only
 
   int limit = n_k;
   if (mask == kMaskKeyPadding) limit = min(max(key_lens[bh / H], 0), n_k);
-  int kend = limit;  // keys this CTA needs
-  if (mask == kMaskCausal) kend = min(kend, min(row0 + ROWS_PER_CTA, n_q));
-
-  float qr[D], acc[D];
-  const float* qp = q + (static_cast<size_t>(bh) * n_q + (valid ? row : 0)) * D;
-#pragma unroll
-  for (int t = 0; t < D; ++t) {
-    qr[t] = valid ? qp[t] * scale_log2 : 0.f;
-    acc[t] = 0.f;
-  }
-  float m = -INFINITY, l = 0.f;
-  const int my_end = mask == kMaskCausal ? min(limit, row + 1) : limit;
+  int end = limit;  // keys [0, end) are visible to this row
+  if (mask == kMaskCausal) end = min(end, row + 1);
+  int cend = limit;  // keys this CTA needs
+  if (mask == kMaskCausal) cend = min(cend, min(row0 + ROWS_PER_CTA, n_q));
+  const int ntiles = (cend + KT - 1) / KT;
 
   const float* kb = k + static_cast<size_t>(bh) * n_k * D;
   const float* vb = v + static_cast<size_t>(bh) * n_k * D;
-  for (int j0 = 0; j0 < kend; j0 += KEYS_PER_TILE) {
-    const int nkeys = min(KEYS_PER_TILE, kend - j0);
-    for (int e = threadIdx.x; e < KEYS_PER_TILE * D; e += ROWS_PER_CTA) {
-      const int jj = e / D, t = e % D;
-      const bool in = jj < nkeys;
-      ks[jj][t] = in ? kb[static_cast<size_t>(j0 + jj) * D + t] : 0.f;
-      vs[jj][t] = in ? vb[static_cast<size_t>(j0 + jj) * D + t] : 0.f;
+  // tile t into buffer t % 2: all 256 threads, 16 bytes each per copy
+  auto load_tile = [&](int t) {
+    const int j0 = t * KT, buf = t & 1;
+#pragma unroll
+    for (int e = threadIdx.x; e < KT * D / 4; e += ROWS_PER_CTA * 32) {
+      const int jj = (4 * e) / D, c = (4 * e) % D;
+      const bool in = j0 + jj < cend;
+      const size_t off = in ? static_cast<size_t>(j0 + jj) * D + c : 0;
+      cp_async16(&sm.k[buf][jj][c], kb + off, in);
+      cp_async16(&sm.v[buf][jj][c], vb + off, in);
     }
-    __syncthreads();
-    if (valid && j0 < my_end) {
-      const int nvis = min(nkeys, my_end - j0);
-      float x[KEYS_PER_TILE];
-      float tmax = -INFINITY;
+    cp_async_commit();
+  };
+  if (ntiles > 0) load_tile(0);
+  if (live) {
+    const float* qp = q + (static_cast<size_t>(bh) * n_q + row) * D;
+    for (int t = lane; t < D; t += 32) sm.q[warp][t] = qp[t] * scale_log2;
+  }
+
+  const int kofs = lane / LPK;        // this lane's key inside a P V step
+  const int c0 = (lane % LPK) * DPL;  // and its first output column
+  float m = -INFINITY, l = 0.f, acc[DPL];
 #pragma unroll
-      for (int jj = 0; jj < KEYS_PER_TILE; ++jj) {
-        float dot = 0.f;
+  for (int c = 0; c < DPL; ++c) acc[c] = 0.f;
+
+  for (int t = 0; t < ntiles; ++t) {
+    // the next tile's copies go out before this one is awaited
+    if (t + 1 < ntiles) {
+      load_tile(t + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();  // tile t (and the queries) visible to every warp
+    const int buf = t & 1, g0 = t * KT;
+    if (live && g0 < end) {
+      // ---- score of key g0 + lane (K row from shared memory, the query
+      // broadcast); four independent partial sums
+      const bool valid = g0 + lane < end;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-        for (int t = 0; t < D; ++t) dot = fmaf(qr[t], ks[jj][t], dot);
-        x[jj] = jj < nvis ? dot : -INFINITY;
-        tmax = fmaxf(tmax, x[jj]);
+      for (int c4 = 0; c4 < D / 4; ++c4) {
+        const float4 kq = *reinterpret_cast<const float4*>(&sm.k[buf][lane][4 * c4]);
+        const float4 qa = *reinterpret_cast<const float4*>(&sm.q[warp][4 * c4]);
+        s0 = fmaf(qa.x, kq.x, s0);
+        s1 = fmaf(qa.y, kq.y, s1);
+        s2 = fmaf(qa.z, kq.z, s2);
+        s3 = fmaf(qa.w, kq.w, s3);
       }
-      const float m_new = fmaxf(m, tmax);
-      const float alpha = exp2f(m - m_new);  // 0 on the first visible tile
+      const float x = valid ? (s0 + s1) + (s2 + s3) : -INFINITY;
+      // ---- streaming softmax over the tile
+      const float mn = fmaxf(m, warp_max(x));
+      const float base = mn == -INFINITY ? 0.f : mn;
+      const float alpha = exp2f(m - base);  // 0 while m = -inf
       l *= alpha;
 #pragma unroll
-      for (int t = 0; t < D; ++t) acc[t] *= alpha;
-      m = m_new;
+      for (int c = 0; c < DPL; ++c) acc[c] *= alpha;
+      m = mn;
+      const float p = exp2f(x - base);  // 0 for keys that are not visible
+      l += p;                           // per-lane partial sum, reduced at the end
+      // ---- P V over the tile's visible keys
+      const int nvis = min(KT, end - g0);
+#pragma unroll 8
+      for (int jj = 0; jj < nvis; jj += KPI) {
+        const int key = jj + kofs;
+        const float pj = __shfl_sync(0xffffffffu, p, key & 31);
+        if (key < nvis) {
 #pragma unroll
-      for (int jj = 0; jj < KEYS_PER_TILE; ++jj) {
-        const float pj = exp2f(x[jj] - m);
-        l += pj;
-#pragma unroll
-        for (int t = 0; t < D; ++t) acc[t] = fmaf(pj, vs[jj][t], acc[t]);
+          for (int c = 0; c < DPL; ++c) acc[c] = fmaf(pj, sm.v[buf][key][c0 + c], acc[c]);
+        }
       }
     }
-    __syncthreads();
+    __syncthreads();  // every warp is done with buffer t % 2 before tile t + 2 lands there
   }
-  if (!valid) return;
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  float* op = o + (static_cast<size_t>(bh) * n_q + row) * D;
+  if (!live) return;
+  // lanes that took other keys of the same P V steps hold the same columns
 #pragma unroll
-  for (int t = 0; t < D; ++t) op[t] = acc[t] * inv;
-  if (lse != nullptr)
-    lse[static_cast<size_t>(bh) * n_q + row] =
-        l > 0.f ? (m + log2f(l)) * 0.693147180559945309f : -INFINITY;
+  for (int c = 0; c < DPL; ++c)
+#pragma unroll
+    for (int xo = LPK; xo < 32; xo <<= 1) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], xo);
+  l = warp_sum(l);
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  if (lane < LPK) {
+    float* op = o + (static_cast<size_t>(bh) * n_q + row) * D + c0;
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) op[c] = acc[c] * inv;
+  }
+  if (lane == 0 && lse != nullptr)
+    lse[static_cast<size_t>(bh) * n_q + row] = l > 0.f ? (m + log2f(l)) * LN2 : -INFINITY;
 }
 
 template <int D>
 cudaError_t launch_d(const Problem& pb, const LaunchCtx& ctx) {
+  const size_t smem = sizeof(F32Smem<D>);
+  cudaError_t err = cudaFuncSetAttribute(attn_fwd_f32_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
   dim3 grid((pb.n_q + ROWS_PER_CTA - 1) / ROWS_PER_CTA, pb.B * pb.H);
-  attn_fwd_f32_kernel<D><<<grid, ROWS_PER_CTA, 0, ctx.stream>>>(
+  attn_fwd_f32_kernel<D><<<grid, ROWS_PER_CTA * 32, smem, ctx.stream>>>(
       static_cast<const float*>(pb.q), static_cast<const float*>(pb.k),
       static_cast<const float*>(pb.v), static_cast<float*>(pb.o), pb.lse, pb.H, pb.n_q,
       pb.n_k, pb.scale * 1.4426950408889634f, pb.mask, pb.key_lens);
