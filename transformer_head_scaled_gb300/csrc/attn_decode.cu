@@ -545,6 +545,41 @@ __global__ void __launch_bounds__(THREADS)
     const int nvalid = min(32, end - g0);
     const long long vstep = KPI * p.sv.n;
     const __nv_bfloat16* vrow = vhead + (g0 + kofs) * p.sv.n + c0;  // advanced by vstep
+    if (nvalid == 32) {
+      // a full group: every value this lane needs is requested before the
+      // first is used (one memory round trip instead of one per key)
+      constexpr int STEPS = 32 / KPI;
+      constexpr int W = (DPL + 1) / 2;  // 32-bit words of DPL bf16 values
+      uint32_t vw[STEPS][W];
+#pragma unroll
+      for (int st = 0; st < STEPS; ++st) {
+        const __nv_bfloat16* vr = vrow + st * vstep;
+        if constexpr (DPL == 4) {
+          const uint2 w2 = __ldg(reinterpret_cast<const uint2*>(vr));
+          vw[st][0] = w2.x;
+          vw[st][1] = w2.y;
+        } else if constexpr (DPL == 2) {
+          vw[st][0] = __ldg(reinterpret_cast<const unsigned int*>(vr));
+        } else {
+          vw[st][0] = __ldg(reinterpret_cast<const unsigned short*>(vr));
+        }
+      }
+#pragma unroll
+      for (int st = 0; st < STEPS; ++st) {
+        const int key = st * KPI + kofs;
+        float vf[DPL];
+#pragma unroll
+        for (int t = 0; t < DPL; ++t)
+          vf[t] = (t & 1) ? bf16hi(vw[st][t / 2]) : bf16lo(vw[st][t / 2]);
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi) {
+          const float pj = __shfl_sync(0xffffffffu, pr[qi], key);
+#pragma unroll
+          for (int t = 0; t < DPL; ++t) o[qi][t] = fmaf(pj, vf[t], o[qi][t]);
+        }
+      }
+      continue;
+    }
     for (int jj = 0; jj < nvalid; jj += KPI, vrow += vstep) {
       const int key = jj + kofs;
       const bool kv = key < nvalid;
