@@ -53,7 +53,7 @@ typedef enum {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = -1, /* null/misaligned pointer, size < 1, bad mask or scale */
-  ATTN_ERR_UNSUPPORTED = -2, /* head size or device this build does not cover */
+  ATTN_ERR_UNSUPPORTED = -2, /* head size or device the library does not cover */
   ATTN_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed, see attn_last_cuda_error */
   ATTN_ERR_TIMEOUT = -4,     /* a kernel gave up on a bounded wait (see attn_check) */
   ATTN_ERR_SCRATCH_TOO_SMALL = -5 /* attn_decode_noalloc: sizes need more than its fixed scratch */
