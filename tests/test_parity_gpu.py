@@ -109,6 +109,16 @@ def test_fp32_masks_and_head_sizes(mask, d):
     _full_case(w, lens=[50, 1] if mask == MASK_KEY_PADDING else None)
 
 
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING])
+@pytest.mark.parametrize("d", [16, 128])
+def test_fp32_many_tiles_and_rows(mask, d):
+    # 33 key tiles of 32 (the double-buffered staging wraps many times, the
+    # last tile ragged), 38 CTAs of 8 rows per head with a ragged last one,
+    # cache lengths on, off and inside tile boundaries
+    w = Workload("f32", 3, 2, 301, 301 if mask == MASK_CAUSAL else 1041, d, mask, "f32")
+    _full_case(w, lens=[1041, 32, 0] if mask == MASK_KEY_PADDING else None)
+
+
 # ------------------------------------------------------------------ bf16 tensor-core path
 
 @pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING])
