@@ -487,7 +487,8 @@ def run_ours(args, w):
                       "unit": "GB/s", "frac": hbm / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                       "traffic": dram_traffic(w), "algorithmic_bytes": hbm,
                       "peak_source": f"{peaks['_source']} hbm_gbs (copy bandwidth)",
-                      "kernel": "attn_decode_split_kernel" + (" + combine" if ws_bytes else "")}),
+                      "kernel": ("attn_decode_split_kernel" if w.d == 64 else "attn_decode_rows_kernel")
+                                + (" + combine" if ws_bytes else "")}),
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": {k2: clk[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons")},
