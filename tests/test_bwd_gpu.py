@@ -185,6 +185,24 @@ def test_bwd_full_size_sampled_heads(name):
         assert dks.abs().max().item() <= 0.05 * dk.float().abs().max().item() * math.sqrt(w.n_k)
 
 
+@pytest.mark.parametrize("name", ["base_enc", "base_dec", "encdec", "base_h16_d32",
+                                  "base_h32_d16", "big"])
+def test_bwd_full_size_whole_tensor(name):
+    """Full-size workloads in the launch configuration the benchmark times,
+    every element of dQ, dK and dV against the oracle (every head: every
+    work item of every persistent CTA)."""
+    w = inputs.WORKLOADS[name]
+    q, k, v, lens = inputs.make_inputs(w, device="cuda")
+    g = inputs.gaussian((w.B, w.h, w.n_q, w.d), 4).to(torch.bfloat16).cuda()
+    o, lse = binding.attn_fwd(q, k, v, scale=w.scale, mask=w.mask, key_lens=lens)
+    dq, dk, dv = binding.attn_bwd(q, k, v, o, lse, g, scale=w.scale, mask=w.mask, key_lens=lens)
+    binding.check()
+    want = oracle.attn_bwd(q.cpu(), k.cpu(), v.cpu(), g.cpu(), w.scale, w.mask,
+                           None if lens is None else lens.cpu().numpy().astype(np.int32))
+    got = [t.float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv)]
+    _compare(got, want)
+
+
 # ---------------------------------------------------------------- restricted window
 
 WINDOW_CASES = [
