@@ -187,7 +187,7 @@ def test_bwd_full_size_sampled_heads(name):
 
 
 @pytest.mark.parametrize("name", ["base_enc", "base_dec", "encdec", "base_h16_d32",
-                                  "base_h32_d16", "big"])
+                                  "base_h32_d16", "big", "big_causal"])
 def test_bwd_full_size_whole_tensor(name):
     """Full-size workloads in the launch configuration the benchmark times,
     every element of dQ, dK and dV against the oracle (every head: every
@@ -253,6 +253,20 @@ def test_bwd_window_full_size_sampled_heads():
     want = oracle.attn_bwd_band(pick(q), pick(k), pick(v), pick(g), w.scale, w.win_left,
                                 w.win_right)
     _compare([pick(t).float().numpy().astype(np.float64) for t in (dq, dk, dv)], want)
+
+
+def test_bwd_window_full_size_whole_tensor():
+    """The restricted-window workload (big model, window of 513 positions),
+    every element of the three gradients against the band oracle."""
+    w = inputs.WORKLOADS["big_window"]
+    q, k, v, _ = inputs.make_inputs(w, device="cuda")
+    g = inputs.gaussian((w.B, w.h, w.n_q, w.d), 4).to(torch.bfloat16).cuda()
+    o, lse = binding.attn_fwd_window(q, k, v, w.win_left, w.win_right)
+    dq, dk, dv = binding.attn_bwd(q, k, v, o, lse, g, window=(w.win_left, w.win_right))
+    binding.check()
+    want = oracle.attn_bwd_band(q.cpu(), k.cpu(), v.cpu(), g.cpu(), w.scale, w.win_left,
+                                w.win_right)
+    _compare([t.float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv)], want)
 
 
 # ---------------------------------------------------------------- other head sizes
