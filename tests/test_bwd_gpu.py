@@ -12,9 +12,9 @@ output itself), each a relative error uniform within +-2^-9, i.e. an rms of
 2^-9/sqrt(3) = 1.1e-3; together about 2.2e-3 relative l2.  REL_L2 allows a
 little over twice that; MAX_REL bounds the largest single deviation, which for
 these Gaussian inputs stays within a few rms of the largest entry.  Small cases
-and six full-size workloads compare every element; the sampled-head cases
-that remain at full size compare whole heads, each head's gradients
-depending only on that head's data.
+and every full-size workload compare every element; the sampled-head cases
+kept beside them compare whole heads, each head's gradients depending only on
+that head's data.
 """
 import math
 
