@@ -5,12 +5,13 @@
 // Need", section 3.2.1, masks of section 3.2.3), for float32 tensors where
 // the tensor-core path's bf16 rounding would not meet a 1e-4 tolerance.  One
 // warp owns one query row and walks its visible keys 32 at a time with a
-// streaming softmax in base 2 (scale*log2(e) folded into the query): for the
-// scores lane l takes key l of the group (its row read with 16-byte loads,
-// the query from shared memory); for P V, LPK = min(d, 32) lanes share one
-// value row, each holding d / LPK consecutive output columns, 32 / LPK keys
-// at a time.  The 8 warps of a CTA (8 query rows of one head) share the K/V
-// tiles, staged in shared memory with asynchronous copies one tile ahead.
+// streaming softmax in base 2 (scale*log2(e) folded into the query).  The 8
+// warps of a CTA (8 query rows of one head) share the K/V tiles of 32 keys,
+// staged in shared memory with asynchronous copies one tile ahead.  For the
+// scores lane l takes key l of the tile (its K row and the query both read
+// from shared memory with 16-byte loads); for P V, LPK = min(d, 32) lanes
+// share one value row, each holding d / LPK consecutive output columns,
+// 32 / LPK keys at a time.
 #include "attn_internal.cuh"
 
 namespace attn {
