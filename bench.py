@@ -449,6 +449,8 @@ def run_ours(args, w):
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
     ms = sum(times) / len(times)
     ms = shard.max_over_ranks(ms, device=dev)
+    ms_median = shard.max_over_ranks(statistics.median(times), device=dev)
+    ms_best = shard.max_over_ranks(min(times), device=dev)
 
     fl = inputs.flops(w)
     fl_alg = inputs.algorithmic_flops(w, kl)
@@ -465,6 +467,7 @@ def run_ours(args, w):
     line = {
         "metric": metric_name(w), "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "ms_median": ms_median, "ms_best": ms_best,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if f32 else "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w), "global_batch": world * w.B,
