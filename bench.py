@@ -311,11 +311,12 @@ def run_reference(args, w):
     per_step_units = max(1, int(n * per_step / max(dt, 1e-9)))
     for _ in range(args.warmup):
         sample(0.0, per_step_units)
-    vals, secs = [], []
+    vals, secs, fls = [], [], []
     for _ in range(args.steps):
-        tf, dt, _, _ = sample(0.0, per_step_units)
+        tf, dt, _, fl = sample(0.0, per_step_units)
         vals.append(tf)
         secs.append(dt)
+        fls.append(fl)
     value = statistics.median(vals)
     cores = cpu_cores_used()
     if bwd:
@@ -331,7 +332,10 @@ def run_reference(args, w):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(w), "l2": "n/a (CPU)"},
+        "config": {"workload": workload_desc(w), "global_batch": w.B,
+                   "parallelism": "host cores of rank 0 (the float64 oracle; no GPU)",
+                   "l2": "n/a (CPU)", "flops_per_step": inputs.flops(w),
+                   "sample_flops_per_step": statistics.median(fls)},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
